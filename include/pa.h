@@ -1,0 +1,180 @@
+/*
+ * libpa — paged decode attention for NVIDIA GB300 (sm_103a), C ABI.
+ *
+ * One decode step of attention for a batch of sequences whose keys and
+ * values live in a paged KV cache addressed through a per-sequence block
+ * table.  Two algorithms compute the same result:
+ *
+ *   V1  one pass over each sequence (one CTA per sequence and KV head);
+ *   V2  the partitioned form of the "paged_attention_v2" commit note
+ *       (project_6, commit 96f4baf "Dockerfile", section "Implementation"):
+ *       Phase 1 computes, for every (sequence, head, partition of
+ *       partition_size tokens), the max logit, the exp-sum and the
+ *       normalised weighted V sum; Phase 2 merges the partitions with the
+ *       log-sum-exp rescale (global max, rescale by exp(m_p - M) times the
+ *       partition's exp-sum, normalised sum of the partials).
+ *
+ * Both reach out[s][h] = softmax_t(scale * q[s][h] . K_t) @ V over the
+ * seq_lens[s] tokens of sequence s, kvh = h / (num_heads / num_kv_heads).
+ *
+ * Layouts (row-major, contiguous, device memory):
+ *   query, out         [num_seqs][num_heads][head_size]          (dtype)
+ *   key_cache,
+ *   value_cache        [num_blocks][num_kv_heads][block_size][head_size]
+ *   block_tables       int32 [num_seqs][max_blocks_per_seq]; entry j of row s
+ *                      is the physical block holding tokens
+ *                      [j*block_size, (j+1)*block_size) of sequence s.
+ *                      Entries past ceil(seq_lens[s]/block_size) are never read.
+ *   seq_lens           int32 [num_seqs], each in [0, max_seq_len]
+ *
+ * Ownership: the caller owns every buffer and the stream.  The library
+ * allocates no device memory, never synchronises in the forward calls, and
+ * only enqueues kernels on `stream` (a cudaStream_t passed as void*; NULL is
+ * the legacy default stream).  Calls on one workspace must not overlap.
+ *
+ * Errors: argument problems are found on the host and returned before any
+ * launch.  A failed launch returns PA_ERR_CUDA (see pa_last_cuda_error).
+ * Problems in the data, found by the kernels (a block-table entry outside
+ * [0, num_blocks), a sequence length outside [0, max_seq_len]) or a bounded
+ * device wait that ran out, are recorded in the workspace's status word and
+ * read with pa_read_device_status.  Kernels never trap.
+ *
+ * Supported: dtype f32, bf16, f16 (query, caches and out share it);
+ * head_size 64, 128, 256; block_size 8, 16, 32, 64; num_heads / num_kv_heads
+ * in [1, 16]; partition_size a multiple of 64 and of block_size, at most
+ * 8192.  K and V caches, query and out 16-byte aligned; workspace 256-byte
+ * aligned; num_blocks * num_kv_heads * block_size < 2^31.
+ */
+#ifndef PA_H_
+#define PA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  PA_OK = 0,
+  PA_ERR_INVALID_ARG = 1,         /* bad pointer, size or combination      */
+  PA_ERR_UNSUPPORTED = 2,         /* legal but not built (dtype, sizes)    */
+  PA_ERR_WORKSPACE_TOO_SMALL = 3, /* workspace_bytes < pa_workspace_bytes  */
+  PA_ERR_CUDA = 4,                /* a CUDA runtime call failed            */
+  PA_ERR_DEVICE_BAD_INPUT = 5,    /* kernel saw a bad block id / length    */
+  PA_ERR_DEVICE_TIMEOUT = 6       /* a bounded device wait ran out         */
+} pa_status_t;
+
+typedef enum { PA_DTYPE_F32 = 0, PA_DTYPE_BF16 = 1, PA_DTYPE_F16 = 2 } pa_dtype_t;
+
+typedef enum { PA_VARIANT_AUTO = 0, PA_VARIANT_V1 = 1, PA_VARIANT_V2 = 2 } pa_variant_t;
+
+/* Arithmetic of QK^T and PV.  AUTO: tensor cores (mma, fp32 accumulate) for
+ * bf16/f16, CUDA-core fp32 FMA for f32.  SIMT forces the CUDA-core path. */
+typedef enum { PA_MATH_AUTO = 0, PA_MATH_SIMT = 1, PA_MATH_TENSOR = 2 } pa_math_t;
+
+/* Optional knobs for pa_forward.  Zero-initialise, then set what you need. */
+typedef struct {
+  int32_t variant;        /* pa_variant_t                                   */
+  int32_t math;           /* pa_math_t                                      */
+  int32_t num_stages;     /* KV pipeline depth per CTA, 0 = library choice  */
+  int32_t debug_flags;    /* PA_DEBUG_*; 0 in production                    */
+  uint64_t wait_limit_ns; /* bound on each device wait, 0 = 1 second        */
+  void *phase1_event;     /* cudaEvent_t or NULL: for V2, recorded on the
+                             stream between the Phase 1 and Phase 2 kernels
+                             (lets a caller time the phases with events)   */
+} pa_options_t;
+
+/* Debug: every consumer warp waits on a barrier that nothing ever releases,
+ * so the bounded wait runs out and the kernel reports PA_ERR_DEVICE_TIMEOUT
+ * (after letting its own in-flight copies land).  Used to test the timeout
+ * path without hanging or faulting the GPU. */
+#define PA_DEBUG_STALL_CONSUMERS 1
+
+/* Bytes of workspace that pa_v2_forward needs (V1 needs only the 256-byte
+ * status block; so does V2 for max_seq_len == 0).  Layout, each part
+ * 256-byte aligned, in this order:
+ *   status      int32 (first 4 bytes of a 256-byte block)
+ *   max_logits  f32 [num_seqs][num_heads][max_parts]   Phase 1 max logit
+ *   exp_sums    f32 [num_seqs][num_heads][max_parts]   sum exp(logit - max)
+ *   tmp_out     f32 [num_seqs][num_heads][max_parts][head_size]  normalised
+ * with max_parts = ceil(max_seq_len / partition_size).  Returns 0 on bad
+ * arguments. */
+size_t pa_workspace_bytes(int num_seqs, int num_heads, int head_size,
+                          int max_seq_len, int partition_size);
+
+/* Byte offsets of the four workspace parts above (offsets[0..3]); returns
+ * PA_ERR_INVALID_ARG on bad arguments.  Lets callers read Phase 1 results. */
+pa_status_t pa_workspace_layout(int num_seqs, int num_heads, int head_size,
+                                int max_seq_len, int partition_size,
+                                size_t offsets[4]);
+
+/* Zero the status word of a new workspace (enqueued on `stream`).  Call once
+ * after allocating it; the kernels only ever write a nonzero code. */
+pa_status_t pa_workspace_init(void *workspace, size_t workspace_bytes,
+                              void *stream);
+
+/* V1: single pass over each whole sequence; one CTA per (sequence, KV head)
+ * computing all num_heads/num_kv_heads query heads of the group with an
+ * online softmax.  partition_size is validated but otherwise unused.
+ * The workspace needs >= 256 bytes (its status block). */
+pa_status_t pa_v1_forward(void *out, const void *query, const void *key_cache,
+                          const void *value_cache, const int32_t *block_tables,
+                          const int32_t *seq_lens, int num_seqs, int num_heads,
+                          int num_kv_heads, int head_size, int num_blocks,
+                          int block_size, int max_blocks_per_seq,
+                          int max_seq_len, float scale, int partition_size,
+                          int dtype, void *workspace, size_t workspace_bytes,
+                          void *stream);
+
+/* V2: Phase 1 kernel with one CTA per (sequence, KV head, partition), writing
+ * max_logits / exp_sums / tmp_out into the workspace, then the Phase 2
+ * log-sum-exp reduce kernel writing out.  Same arguments as V1; the
+ * workspace must hold pa_workspace_bytes(...) bytes. */
+pa_status_t pa_v2_forward(void *out, const void *query, const void *key_cache,
+                          const void *value_cache, const int32_t *block_tables,
+                          const int32_t *seq_lens, int num_seqs, int num_heads,
+                          int num_kv_heads, int head_size, int num_blocks,
+                          int block_size, int max_blocks_per_seq,
+                          int max_seq_len, float scale, int partition_size,
+                          int dtype, void *workspace, size_t workspace_bytes,
+                          void *stream);
+
+/* The same call with the V1/V2 choice made by pa_choose_v2 (the device's SM
+ * count is queried once per device), or forced through `opts` (NULL = all
+ * defaults).  For V2 the workspace must hold pa_workspace_bytes(...). */
+pa_status_t pa_forward(void *out, const void *query, const void *key_cache,
+                       const void *value_cache, const int32_t *block_tables,
+                       const int32_t *seq_lens, int num_seqs, int num_heads,
+                       int num_kv_heads, int head_size, int num_blocks,
+                       int block_size, int max_blocks_per_seq, int max_seq_len,
+                       float scale, int partition_size, int dtype,
+                       void *workspace, size_t workspace_bytes, void *stream,
+                       const pa_options_t *opts);
+
+/* Host heuristic: 1 if V2 should serve this batch on a GPU with sm_count
+ * SMs, 0 for V1.  V1 when every sequence fits in one partition; otherwise V2
+ * unless the batch alone fills the GPU several times over with short
+ * sequences (the commit note's V1 range of seq_len <= 8192, scaled by how
+ * many (sequence, KV head) CTAs there are per SM). */
+int pa_choose_v2(int num_seqs, int num_kv_heads, int max_seq_len,
+                 int partition_size, int sm_count);
+
+/* Synchronise `stream`, return the workspace's status word as a pa_status_t
+ * (PA_OK if no kernel reported a problem) and reset it to 0. */
+pa_status_t pa_read_device_status(void *workspace, void *stream);
+
+/* Static English text for a status code. */
+const char *pa_status_string(int status);
+
+/* Text of the last CUDA error seen by this thread inside the library. */
+const char *pa_last_cuda_error(void);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int pa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_H_ */

@@ -1,0 +1,516 @@
+// libpa C ABI: argument checks, the V1/V2 choice, the launch plan (pipeline
+// depth, grids, TMA descriptors) and the kernel launches.
+#include <cudaTypedefs.h>
+#include <math.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "pa.h"
+#include "pa_internal.h"
+
+namespace {
+
+using namespace pa;
+
+thread_local char g_last_error[512] = "";
+
+pa_status_t fail_cuda(const char *what, const char *detail) {
+  snprintf(g_last_error, sizeof g_last_error, "%s: %s", what, detail);
+  return PA_ERR_CUDA;
+}
+pa_status_t fail_cuda(const char *what, cudaError_t e) {
+  return fail_cuda(what, cudaGetErrorString(e));
+}
+
+int ilog2(int x) {
+  int r = 0;
+  while ((1 << r) < x) ++r;
+  return r;
+}
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+int elt_size(int dtype) { return dtype == PA_DTYPE_F32 ? 4 : 2; }
+
+// ---------------------------------------------------------------------------
+// Per-device facts, queried once.
+struct DeviceFacts {
+  bool ready = false;
+  int sm_count = 0;
+  int max_smem_optin = 0;
+};
+constexpr int kMaxDevices = 64;
+DeviceFacts g_devices[kMaxDevices];
+std::mutex g_mutex;
+
+pa_status_t device_facts(DeviceFacts **out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail_cuda("cudaGetDevice", e);
+  if (dev < 0 || dev >= kMaxDevices) return fail_cuda("cudaGetDevice", "device ordinal too large");
+  std::lock_guard<std::mutex> lock(g_mutex);
+  DeviceFacts &f = g_devices[dev];
+  if (!f.ready) {
+    e = cudaDeviceGetAttribute(&f.sm_count, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return fail_cuda("cudaDeviceGetAttribute(SM count)", e);
+    e = cudaDeviceGetAttribute(&f.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (e != cudaSuccess) return fail_cuda("cudaDeviceGetAttribute(smem)", e);
+    f.ready = true;
+  }
+  *out = &f;
+  return PA_OK;
+}
+
+// Raise a kernel's dynamic shared-memory limit once per (kernel, device).
+struct SmemSetting {
+  const void *fn;
+  int dev;
+  int bytes;
+};
+SmemSetting g_smem_settings[256];
+int g_num_smem_settings = 0;
+
+pa_status_t ensure_smem(const void *fn, size_t bytes) {
+  if (bytes <= 48 * 1024) return PA_OK;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail_cuda("cudaGetDevice", e);
+  std::lock_guard<std::mutex> lock(g_mutex);
+  for (int i = 0; i < g_num_smem_settings; ++i)
+    if (g_smem_settings[i].fn == fn && g_smem_settings[i].dev == dev &&
+        g_smem_settings[i].bytes >= (int)bytes)
+      return PA_OK;
+  e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e != cudaSuccess) return fail_cuda("cudaFuncSetAttribute(max dynamic smem)", e);
+  for (int i = 0; i < g_num_smem_settings; ++i)
+    if (g_smem_settings[i].fn == fn && g_smem_settings[i].dev == dev) {
+      g_smem_settings[i].bytes = (int)bytes;
+      return PA_OK;
+    }
+  if (g_num_smem_settings < 256) g_smem_settings[g_num_smem_settings++] = {fn, dev, (int)bytes};
+  return PA_OK;
+}
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no
+// link-time dependency on libcuda).
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+pa_status_t get_encoder(PFN_cuTensorMapEncodeTiled_v12000 *fn) {
+  std::lock_guard<std::mutex> lock(g_mutex);
+  if (!g_encode) {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                                     cudaEnableDefault, &q);
+    if (e != cudaSuccess) return fail_cuda("cudaGetDriverEntryPointByVersion", e);
+    if (q != cudaDriverEntryPointSuccess || !p)
+      return fail_cuda("cudaGetDriverEntryPointByVersion", "cuTensorMapEncodeTiled not found");
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  *fn = g_encode;
+  return PA_OK;
+}
+
+// A 2-D view of a cache: rows = num_blocks * num_kv_heads * block_size token
+// rows of head_size elements; the box is one 128-byte panel x unit_rows rows,
+// landing in shared memory with the 128-byte swizzle.
+pa_status_t encode_cache_map(CUtensorMap *map, const void *base, int dtype, int head_size,
+                             long long rows, int unit_rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc;
+  pa_status_t st = get_encoder(&enc);
+  if (st != PA_OK) return st;
+  const int elt = elt_size(dtype);
+  CUtensorMapDataType dt = dtype == PA_DTYPE_F32    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                           : dtype == PA_DTYPE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                    : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  cuuint64_t gdim[2] = {(cuuint64_t)head_size, (cuuint64_t)rows};
+  cuuint64_t gstride[1] = {(cuuint64_t)head_size * elt};
+  cuuint32_t box[2] = {(cuuint32_t)(kPanelBytes / elt), (cuuint32_t)unit_rows};
+  cuuint32_t estride[2] = {1, 1};
+  CUresult r = enc(map, dt, 2, const_cast<void *>(base), gdim, gstride, box, estride,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    char msg[64];
+    snprintf(msg, sizeof msg, "CUresult %d", (int)r);
+    return fail_cuda("cuTensorMapEncodeTiled", msg);
+  }
+  return PA_OK;
+}
+
+// ---------------------------------------------------------------------------
+struct Call {
+  void *out;
+  const void *query, *key_cache, *value_cache;
+  const int32_t *block_tables, *seq_lens;
+  int num_seqs, num_heads, num_kv_heads, head_size, num_blocks, block_size;
+  int max_blocks_per_seq, max_seq_len;
+  float scale;
+  int partition_size, dtype;
+  void *workspace;
+  size_t workspace_bytes;
+  cudaStream_t stream;
+};
+
+int max_parts_of(int max_seq_len, int partition_size) {
+  return (max_seq_len + partition_size - 1) / partition_size;
+}
+
+constexpr int kMaxReduceParts = 40000;  // Phase 2 keeps one weight per partition in smem
+
+// Checks that need no device.  need_v2: the workspace must hold the partials.
+pa_status_t check_args(const Call &c, bool need_v2) {
+  if (c.dtype != PA_DTYPE_F32 && c.dtype != PA_DTYPE_BF16 && c.dtype != PA_DTYPE_F16)
+    return PA_ERR_INVALID_ARG;
+  if (c.num_seqs < 0 || c.num_heads < 1 || c.num_kv_heads < 1 || c.num_blocks < 1 ||
+      c.max_blocks_per_seq < 1 || c.max_seq_len < 0 || c.block_size < 1 || c.partition_size < 1)
+    return PA_ERR_INVALID_ARG;
+  if (c.num_heads % c.num_kv_heads) return PA_ERR_INVALID_ARG;
+  if (!isfinite(c.scale)) return PA_ERR_INVALID_ARG;
+  if ((long long)c.max_seq_len > (long long)c.max_blocks_per_seq * c.block_size)
+    return PA_ERR_INVALID_ARG;
+  if (c.head_size != 64 && c.head_size != 128 && c.head_size != 256) return PA_ERR_UNSUPPORTED;
+  if (c.block_size != 8 && c.block_size != 16 && c.block_size != 32 && c.block_size != 64)
+    return PA_ERR_UNSUPPORTED;
+  if (c.num_heads / c.num_kv_heads > 16) return PA_ERR_UNSUPPORTED;
+  if (c.partition_size % 64 || c.partition_size % c.block_size || c.partition_size > 8192)
+    return PA_ERR_UNSUPPORTED;
+  if ((long long)c.num_blocks * c.num_kv_heads * c.block_size >= (1ll << 31))
+    return PA_ERR_UNSUPPORTED;
+  if ((long long)c.num_seqs * c.num_kv_heads * max_parts_of(c.max_seq_len, c.partition_size) >=
+      (1ll << 31))
+    return PA_ERR_UNSUPPORTED;
+  if (need_v2 && max_parts_of(c.max_seq_len, c.partition_size) > kMaxReduceParts)
+    return PA_ERR_UNSUPPORTED;
+  if (!c.out || !c.query || !c.key_cache || !c.value_cache || !c.block_tables || !c.seq_lens ||
+      !c.workspace)
+    return PA_ERR_INVALID_ARG;
+  if (!aligned(c.out, 16) || !aligned(c.query, 16) || !aligned(c.key_cache, 16) ||
+      !aligned(c.value_cache, 16) || !aligned(c.block_tables, 4) || !aligned(c.seq_lens, 4) ||
+      !aligned(c.workspace, 256))
+    return PA_ERR_INVALID_ARG;
+  const size_t need = need_v2 ? pa_workspace_bytes(c.num_seqs, c.num_heads, c.head_size,
+                                                   c.max_seq_len, c.partition_size)
+                              : (size_t)kStatusBytes;
+  if (need == 0) return PA_ERR_INVALID_ARG;
+  if (c.workspace_bytes < need) return PA_ERR_WORKSPACE_TOO_SMALL;
+  return PA_OK;
+}
+
+AttnKernelInfo pick_kernel(int math, int dtype, int head_size, int group) {
+  if (math == kMathTensor) {
+    if (dtype == PA_DTYPE_BF16) return attn_kernel_tensor_bf16(head_size, group);
+    if (dtype == PA_DTYPE_F16) return attn_kernel_tensor_f16(head_size, group);
+  } else {
+    if (dtype == PA_DTYPE_F32) return attn_kernel_simt_f32(head_size, group);
+    if (dtype == PA_DTYPE_BF16) return attn_kernel_simt_bf16(head_size, group);
+    if (dtype == PA_DTYPE_F16) return attn_kernel_simt_f16(head_size, group);
+  }
+  return AttnKernelInfo{nullptr, 0, 0, 0};
+}
+
+// Default pipeline depth: about 96 KB of K+V stages per CTA, so that two
+// CTAs share an SM and each keeps 64 KB or more of loads in flight.
+int default_stages(size_t stage_bytes) {
+  int n = (int)((96 * 1024) / stage_bytes);
+  return n < 2 ? 2 : (n > 8 ? 8 : n);
+}
+
+pa_status_t launch(const Call &c, bool v2, const pa_options_t &opt) {
+  DeviceFacts *dev = nullptr;
+  pa_status_t st = device_facts(&dev);
+  if (st != PA_OK) return st;
+
+  const int group = c.num_heads / c.num_kv_heads;
+  int math = opt.math;
+  if (math == PA_MATH_AUTO) math = c.dtype == PA_DTYPE_F32 ? kMathSimt : kMathTensor;
+  if (math != kMathSimt && math != kMathTensor) return PA_ERR_INVALID_ARG;
+  if (math == kMathTensor && c.dtype == PA_DTYPE_F32) return PA_ERR_UNSUPPORTED;
+  const AttnKernelInfo k = pick_kernel(math, c.dtype, c.head_size, group);
+  if (!k.fn) return PA_ERR_UNSUPPORTED;
+
+  const int elt = elt_size(c.dtype);
+  const size_t stage_bytes = (size_t)k.stage_tokens * c.head_size * elt * 2;
+  int stages = opt.num_stages > 0 ? opt.num_stages : default_stages(stage_bytes);
+  if (stages < 2 || stages > 16) return PA_ERR_INVALID_ARG;
+  const bool simt = math == kMathSimt;
+  size_t smem = attn_smem_bytes(c.head_size, elt, k.consumer_warps, k.max_group, stages, simt);
+  while (smem > (size_t)dev->max_smem_optin && stages > 2 && opt.num_stages <= 0) {
+    --stages;
+    smem = attn_smem_bytes(c.head_size, elt, k.consumer_warps, k.max_group, stages, simt);
+  }
+  if (smem > (size_t)dev->max_smem_optin) return PA_ERR_UNSUPPORTED;
+
+  const int unit_rows = c.block_size < k.stage_tokens ? c.block_size : k.stage_tokens;
+  const long long rows = (long long)c.num_blocks * c.num_kv_heads * c.block_size;
+  CUtensorMap tmap_k, tmap_v;
+  st = encode_cache_map(&tmap_k, c.key_cache, c.dtype, c.head_size, rows, unit_rows);
+  if (st != PA_OK) return st;
+  st = encode_cache_map(&tmap_v, c.value_cache, c.dtype, c.head_size, rows, unit_rows);
+  if (st != PA_OK) return st;
+
+  uint8_t *ws = static_cast<uint8_t *>(c.workspace);
+  const int max_parts = v2 ? max_parts_of(c.max_seq_len, c.partition_size) : 1;
+  size_t off[4] = {0, 0, 0, 0};
+  if (v2) {
+    if (pa_workspace_layout(c.num_seqs, c.num_heads, c.head_size, c.max_seq_len,
+                            c.partition_size, off) != PA_OK)
+      return PA_ERR_INVALID_ARG;
+  }
+
+  AttnParams p;
+  memset(&p, 0, sizeof p);
+  p.query = c.query;
+  p.out = c.out;
+  p.block_tables = c.block_tables;
+  p.seq_lens = c.seq_lens;
+  p.status = reinterpret_cast<int *>(ws);
+  if (v2) {
+    p.max_logits = reinterpret_cast<float *>(ws + off[1]);
+    p.exp_sums = reinterpret_cast<float *>(ws + off[2]);
+    p.tmp_out = reinterpret_cast<float *>(ws + off[3]);
+  }
+  p.num_seqs = c.num_seqs;
+  p.num_heads = c.num_heads;
+  p.num_kv_heads = c.num_kv_heads;
+  p.group = group;
+  p.block_size = c.block_size;
+  p.log2_block_size = ilog2(c.block_size);
+  p.unit_rows = unit_rows;
+  p.log2_unit_rows = ilog2(unit_rows);
+  p.max_blocks_per_seq = c.max_blocks_per_seq;
+  p.max_seq_len = c.max_seq_len;
+  p.num_blocks = c.num_blocks;
+  p.range_tokens = v2 ? c.partition_size : (c.max_seq_len > 0 ? c.max_seq_len : 1);
+  p.max_parts = max_parts > 0 ? max_parts : 1;
+  p.write_partials = v2 ? 1 : 0;
+  p.num_stages = stages;
+  p.debug_flags = opt.debug_flags;
+  p.scale_log2 = (float)((double)c.scale * 1.4426950408889634);
+  p.wait_limit_ns = opt.wait_limit_ns ? opt.wait_limit_ns : kDefaultWaitLimitNs;
+
+  st = ensure_smem(k.fn, smem);
+  if (st != PA_OK) return st;
+
+  const long long grid = (long long)c.num_seqs * c.num_kv_heads * p.max_parts;
+  if (grid > 0) {
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof cfg);
+    cfg.gridDim = dim3((unsigned)grid, 1, 1);
+    cfg.blockDim = dim3((unsigned)((k.consumer_warps + 1) * 32), 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = c.stream;
+    void *args[3] = {&p, &tmap_k, &tmap_v};
+    cudaError_t e = cudaLaunchKernelExC(&cfg, k.fn, args);
+    if (e != cudaSuccess) return fail_cuda("launch attention kernel", e);
+  }
+  if (!v2) return PA_OK;
+  if (opt.phase1_event) {
+    cudaError_t e = cudaEventRecord(static_cast<cudaEvent_t>(opt.phase1_event), c.stream);
+    if (e != cudaSuccess) return fail_cuda("cudaEventRecord(phase1_event)", e);
+  }
+
+  // ---- Phase 2 (chained with programmatic dependent launch)
+  ReduceParams r;
+  memset(&r, 0, sizeof r);
+  r.out = c.out;
+  r.max_logits = p.max_logits;
+  r.exp_sums = p.exp_sums;
+  r.tmp_out = p.tmp_out;
+  r.seq_lens = c.seq_lens;
+  r.status = p.status;
+  r.num_seqs = c.num_seqs;
+  r.num_heads = c.num_heads;
+  r.head_size = c.head_size;
+  r.max_parts = p.max_parts;
+  r.partition_size = c.partition_size;
+  r.max_seq_len = c.max_seq_len;
+  const long long pairs = (long long)c.num_seqs * c.num_heads;
+  const int dsplit = pairs < 2LL * dev->sm_count ? c.head_size / 32 : 1;
+  r.cols_per_cta = c.head_size / dsplit;
+  const void *rfn = reduce_kernel(c.dtype);
+  const size_t rsmem = 256 * 16 + (size_t)p.max_parts * 4;
+  st = ensure_smem(rfn, rsmem);
+  if (st != PA_OK) return st;
+  if (pairs == 0) return PA_OK;
+  cudaLaunchConfig_t cfg;
+  memset(&cfg, 0, sizeof cfg);
+  cfg.gridDim = dim3((unsigned)pairs, (unsigned)dsplit, 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.dynamicSmemBytes = rsmem;
+  cfg.stream = c.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  void *rargs[1] = {&r};
+  cudaError_t e = cudaLaunchKernelExC(&cfg, rfn, rargs);
+  if (e != cudaSuccess) return fail_cuda("launch reduce kernel", e);
+  return PA_OK;
+}
+
+Call make_call(void *out, const void *query, const void *key_cache, const void *value_cache,
+               const int32_t *block_tables, const int32_t *seq_lens, int num_seqs, int num_heads,
+               int num_kv_heads, int head_size, int num_blocks, int block_size,
+               int max_blocks_per_seq, int max_seq_len, float scale, int partition_size,
+               int dtype, void *workspace, size_t workspace_bytes, void *stream) {
+  return Call{out,          query,         key_cache,          value_cache, block_tables,
+              seq_lens,     num_seqs,      num_heads,          num_kv_heads, head_size,
+              num_blocks,   block_size,    max_blocks_per_seq, max_seq_len, scale,
+              partition_size, dtype,       workspace,          workspace_bytes,
+              static_cast<cudaStream_t>(stream)};
+}
+
+pa_status_t run(const Call &c, int variant, const pa_options_t &opt) {
+  bool v2;
+  if (variant == PA_VARIANT_V1) {
+    v2 = false;
+  } else if (variant == PA_VARIANT_V2) {
+    v2 = true;
+  } else if (variant == PA_VARIANT_AUTO) {
+    pa_status_t st0 = check_args(c, false);
+    if (st0 != PA_OK) return st0;
+    if (c.num_seqs == 0) return PA_OK;
+    DeviceFacts *dev = nullptr;
+    pa_status_t st = device_facts(&dev);
+    if (st != PA_OK) return st;
+    v2 = pa_choose_v2(c.num_seqs, c.num_kv_heads, c.max_seq_len, c.partition_size,
+                      dev->sm_count) != 0;
+  } else {
+    return PA_ERR_INVALID_ARG;
+  }
+  pa_status_t st = check_args(c, v2);
+  if (st != PA_OK) return st;
+  if (c.num_seqs == 0) return PA_OK;
+  return launch(c, v2, opt);
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t pa_workspace_bytes(int num_seqs, int num_heads, int head_size, int max_seq_len,
+                          int partition_size) {
+  size_t off[4];
+  if (pa_workspace_layout(num_seqs, num_heads, head_size, max_seq_len, partition_size, off) !=
+      PA_OK)
+    return 0;
+  const size_t parts = (size_t)max_parts_of(max_seq_len, partition_size);
+  return off[3] + align256((size_t)num_seqs * num_heads * parts * head_size * 4);
+}
+
+pa_status_t pa_workspace_layout(int num_seqs, int num_heads, int head_size, int max_seq_len,
+                                int partition_size, size_t offsets[4]) {
+  if (!offsets || num_seqs < 0 || num_heads < 1 || head_size < 1 || max_seq_len < 0 ||
+      partition_size < 1)
+    return PA_ERR_INVALID_ARG;
+  const size_t parts = (size_t)max_parts_of(max_seq_len, partition_size);
+  const size_t stats = align256((size_t)num_seqs * num_heads * parts * 4);
+  offsets[0] = 0;
+  offsets[1] = kStatusBytes;
+  offsets[2] = offsets[1] + stats;
+  offsets[3] = offsets[2] + stats;
+  return PA_OK;
+}
+
+pa_status_t pa_workspace_init(void *workspace, size_t workspace_bytes, void *stream) {
+  if (!workspace || workspace_bytes < (size_t)kStatusBytes || !aligned(workspace, 256))
+    return PA_ERR_INVALID_ARG;
+  cudaError_t e = cudaMemsetAsync(workspace, 0, kStatusBytes, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail_cuda("cudaMemsetAsync(status)", e);
+  return PA_OK;
+}
+
+pa_status_t pa_v1_forward(void *out, const void *query, const void *key_cache,
+                          const void *value_cache, const int32_t *block_tables,
+                          const int32_t *seq_lens, int num_seqs, int num_heads, int num_kv_heads,
+                          int head_size, int num_blocks, int block_size, int max_blocks_per_seq,
+                          int max_seq_len, float scale, int partition_size, int dtype,
+                          void *workspace, size_t workspace_bytes, void *stream) {
+  pa_options_t opt;
+  memset(&opt, 0, sizeof opt);
+  return run(make_call(out, query, key_cache, value_cache, block_tables, seq_lens, num_seqs,
+                       num_heads, num_kv_heads, head_size, num_blocks, block_size,
+                       max_blocks_per_seq, max_seq_len, scale, partition_size, dtype, workspace,
+                       workspace_bytes, stream),
+             PA_VARIANT_V1, opt);
+}
+
+pa_status_t pa_v2_forward(void *out, const void *query, const void *key_cache,
+                          const void *value_cache, const int32_t *block_tables,
+                          const int32_t *seq_lens, int num_seqs, int num_heads, int num_kv_heads,
+                          int head_size, int num_blocks, int block_size, int max_blocks_per_seq,
+                          int max_seq_len, float scale, int partition_size, int dtype,
+                          void *workspace, size_t workspace_bytes, void *stream) {
+  pa_options_t opt;
+  memset(&opt, 0, sizeof opt);
+  return run(make_call(out, query, key_cache, value_cache, block_tables, seq_lens, num_seqs,
+                       num_heads, num_kv_heads, head_size, num_blocks, block_size,
+                       max_blocks_per_seq, max_seq_len, scale, partition_size, dtype, workspace,
+                       workspace_bytes, stream),
+             PA_VARIANT_V2, opt);
+}
+
+pa_status_t pa_forward(void *out, const void *query, const void *key_cache,
+                       const void *value_cache, const int32_t *block_tables,
+                       const int32_t *seq_lens, int num_seqs, int num_heads, int num_kv_heads,
+                       int head_size, int num_blocks, int block_size, int max_blocks_per_seq,
+                       int max_seq_len, float scale, int partition_size, int dtype,
+                       void *workspace, size_t workspace_bytes, void *stream,
+                       const pa_options_t *opts) {
+  pa_options_t opt;
+  memset(&opt, 0, sizeof opt);
+  if (opts) opt = *opts;
+  return run(make_call(out, query, key_cache, value_cache, block_tables, seq_lens, num_seqs,
+                       num_heads, num_kv_heads, head_size, num_blocks, block_size,
+                       max_blocks_per_seq, max_seq_len, scale, partition_size, dtype, workspace,
+                       workspace_bytes, stream),
+             opt.variant, opt);
+}
+
+int pa_choose_v2(int num_seqs, int num_kv_heads, int max_seq_len, int partition_size,
+                 int sm_count) {
+  if (partition_size < 1 || max_seq_len <= partition_size) return 0;
+  const long long v1_ctas = (long long)num_seqs * num_kv_heads;
+  // V1 only when its one-CTA-per-(sequence, KV head) grid already covers the
+  // GPU several times over and no sequence is long enough to unbalance it.
+  if (max_seq_len <= 8192 && sm_count > 0 && v1_ctas >= 8LL * sm_count) return 0;
+  return 1;
+}
+
+pa_status_t pa_read_device_status(void *workspace, void *stream) {
+  if (!workspace || !aligned(workspace, 256)) return PA_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return fail_cuda("cudaStreamSynchronize", e);
+  int v = 0;
+  e = cudaMemcpy(&v, workspace, sizeof v, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return fail_cuda("cudaMemcpy(status)", e);
+  if (v != 0) {
+    e = cudaMemset(workspace, 0, sizeof v);
+    if (e != cudaSuccess) return fail_cuda("cudaMemset(status)", e);
+  }
+  return static_cast<pa_status_t>(v);
+}
+
+const char *pa_status_string(int status) {
+  switch (status) {
+    case PA_OK: return "ok";
+    case PA_ERR_INVALID_ARG: return "invalid argument";
+    case PA_ERR_UNSUPPORTED: return "unsupported configuration";
+    case PA_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case PA_ERR_CUDA: return "CUDA error";
+    case PA_ERR_DEVICE_BAD_INPUT: return "kernel found a bad block-table entry or sequence length";
+    case PA_ERR_DEVICE_TIMEOUT: return "a bounded device wait ran out";
+  }
+  return "unknown status";
+}
+
+const char *pa_last_cuda_error(void) { return g_last_error; }
+
+int pa_version(void) { return 100; }
+
+}  // extern "C"

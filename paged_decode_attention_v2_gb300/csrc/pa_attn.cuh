@@ -1,0 +1,645 @@
+// Paged decode attention kernel: V1 (whole sequence per CTA) and Phase 1 of
+// V2 (one partition per CTA), per the "paged_attention_v2" commit note
+// (project_6, commit 96f4baf "Dockerfile", section "Implementation",
+// "Phase 1: Per-partition attention").
+//
+// One CTA = one (sequence, KV head, token range).  It computes all G query
+// heads that share the KV head, so every K/V byte of the range crosses HBM
+// once.  Warp roles:
+//   warp NW        producer: reads the block table and issues TMA tile loads
+//                  of whole KV pages (128-byte swizzled panels) into a ring
+//                  of shared-memory stages, completing on mbarriers;
+//   warps 0..NW-1  consumers: each takes 16 tokens of every stage and keeps
+//                  its own online-softmax state (running max, sum, output).
+// At the end the consumer warps merge their states (the same log-sum-exp
+// combine as Phase 2) and write either the final output (V1) or the
+// partition's max_logits / exp_sums / normalised tmp_output (V2 Phase 1).
+//
+// Every wait is bounded (%globaltimer); a wait that runs out records
+// PA_ERR_DEVICE_TIMEOUT, the CTA lets its own in-flight copies land, and
+// returns without writing results.
+#pragma once
+
+#include <math_constants.h>
+
+#include <type_traits>
+
+#include "pa_device.cuh"
+
+namespace pa {
+
+constexpr int kStatusBadInput = 5;  // PA_ERR_DEVICE_BAD_INPUT
+constexpr int kStatusTimeout = 6;   // PA_ERR_DEVICE_TIMEOUT
+constexpr int kDebugStallConsumers = 1;
+
+// Geometry of one K (or V) stage buffer as TMA writes it:
+//   [unit][panel][unit_rows][128 bytes]
+// where a unit is unit_rows consecutive tokens of one page, a panel is a
+// 128-byte slice of the head dimension, and inside every 1024 bytes the
+// 16-byte chunk index is XOR-ed with the row index mod 8 (TMA 128B swizzle).
+struct StageGeom {
+  int log2_unit_rows;
+  int unit_rows_mask;
+  uint32_t panel_bytes;  // unit_rows * 128
+  uint32_t unit_bytes;   // panels * unit_rows * 128
+
+  __device__ __forceinline__ uint32_t row_addr(uint32_t base, int tok) const {
+    return base + (uint32_t)(tok >> log2_unit_rows) * unit_bytes +
+           ((uint32_t)(tok & unit_rows_mask) << 7);
+  }
+  // 16-byte chunk `chunk` of the row that starts at row_addr(.., tok).
+  __device__ __forceinline__ uint32_t chunk_addr(uint32_t row, int tok, int chunk) const {
+    return row + (uint32_t)(chunk >> 3) * panel_bytes + ((uint32_t)((chunk & 7) ^ (tok & 7)) << 4);
+  }
+};
+
+// ---------------------------------------------------------------------------
+// Tensor-core math (bf16 / f16): per 16-token tile,
+//   S^T[16 tok][8 heads] = K[16 tok][D] . Q^T[D][8 heads]     (mma m16n8k16)
+//   O^T[D][8 heads]     += V^T[D][16 tok] . P^T[16 tok][8 heads]
+// Q^T fragments stay in registers for the whole range; K comes in through
+// ldmatrix, V through ldmatrix.trans, and P^T is turned from the S^T
+// accumulator layout into the B-operand layout with movmatrix.trans.
+// Accumulation is fp32.  P is rounded to the input type for the PV product
+// and the running sum adds the rounded values, so the weights used and the
+// normaliser agree.
+template <typename T, int D, int NT>
+struct TensorMath {
+  static constexpr int KS = D / 16;
+  static constexpr int GMAX = 8 * NT;
+  uint32_t qf[NT][KS][2];
+  float o[NT][KS][4];
+  float m[NT][2];
+  float l[NT][2];
+
+  __device__ __forceinline__ void init(const AttnParams &p, int s, int kvh, int lane, float *,
+                                       float *) {
+    const T *q = static_cast<const T *>(p.query) +
+                 ((size_t)s * p.num_heads + (size_t)kvh * p.group) * D;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const int h = nt * 8 + (lane >> 2);
+      const bool live = h < p.group;
+#pragma unroll
+      for (int ks = 0; ks < KS; ++ks) {
+        const T *src = q + (size_t)h * D + ks * 16 + 2 * (lane & 3);
+        qf[nt][ks][0] = live ? *reinterpret_cast<const uint32_t *>(src) : 0u;
+        qf[nt][ks][1] = live ? *reinterpret_cast<const uint32_t *>(src + 8) : 0u;
+      }
+#pragma unroll
+      for (int mt = 0; mt < KS; ++mt)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) o[nt][mt][j] = 0.f;
+      m[nt][0] = m[nt][1] = -CUDART_INF_F;
+      l[nt][0] = l[nt][1] = 0.f;
+    }
+  }
+
+  __device__ __forceinline__ void tile(uint32_t kbase, uint32_t vbase, const StageGeom &g, int tok0,
+                                       int valid, int lane, float scale_log2) {
+    const int mi = lane >> 3, r = lane & 7;
+    // ---- S^T = K Q^T
+    float sacc[NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) sacc[nt][j] = 0.f;
+    {
+      const int tokA = tok0 + r + ((mi & 1) << 3);
+      const uint32_t rowA = g.row_addr(kbase, tokA);
+#pragma unroll
+      for (int ks = 0; ks < KS; ++ks) {
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4(g.chunk_addr(rowA, tokA, 2 * ks + (mi >> 1)), a0, a1, a2, a3);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+          MmaOp<T>::run(sacc[nt], a0, a1, a2, a3, qf[nt][ks][0], qf[nt][ks][1]);
+      }
+    }
+    // ---- online softmax on the tile (log2 domain)
+    const int t_lo = lane >> 2, t_hi = t_lo + 8;
+    uint32_t pb[NT][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      float x0 = sacc[nt][0] * scale_log2, x1 = sacc[nt][1] * scale_log2;
+      float x2 = sacc[nt][2] * scale_log2, x3 = sacc[nt][3] * scale_log2;
+      if (t_lo >= valid) x0 = x1 = -CUDART_INF_F;
+      if (t_hi >= valid) x2 = x3 = -CUDART_INF_F;
+      float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) {
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+      }
+      const float mn0 = fmaxf(m[nt][0], mx0), mn1 = fmaxf(m[nt][1], mx1);
+      const float al0 = exp2f(m[nt][0] - mn0), al1 = exp2f(m[nt][1] - mn1);
+      const uint32_t plo = MmaOp<T>::pack(exp2f(x0 - mn0), exp2f(x1 - mn1));
+      const uint32_t phi = MmaOp<T>::pack(exp2f(x2 - mn0), exp2f(x3 - mn1));
+      const float2 flo = MmaOp<T>::unpack(plo), fhi = MmaOp<T>::unpack(phi);
+      l[nt][0] = l[nt][0] * al0 + (flo.x + fhi.x);
+      l[nt][1] = l[nt][1] * al1 + (flo.y + fhi.y);
+      m[nt][0] = mn0;
+      m[nt][1] = mn1;
+      pb[nt][0] = movmatrix_trans(plo);
+      pb[nt][1] = movmatrix_trans(phi);
+#pragma unroll
+      for (int mt = 0; mt < KS; ++mt) {
+        o[nt][mt][0] *= al0;
+        o[nt][mt][1] *= al1;
+        o[nt][mt][2] *= al0;
+        o[nt][mt][3] *= al1;
+      }
+    }
+    // ---- rows past the end of the range hold stale or foreign data: zero
+    // them so that 0-weight x NaN cannot reach the accumulator.
+    if (valid < 16) {
+      constexpr int CPR = D * (int)sizeof(T) / 16;  // chunks per row
+      const int n = (16 - valid) * CPR;
+      for (int c = lane; c < n; c += 32) {
+        const int tok = tok0 + valid + c / CPR;
+        const uint32_t a = g.chunk_addr(g.row_addr(vbase, tok), tok, c % CPR);
+        asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" ::"r"(a), "r"(0u) : "memory");
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+    }
+    // ---- O^T += V^T P^T
+    {
+      const int tokB = tok0 + r + ((mi >> 1) << 3);
+      const uint32_t rowB = g.row_addr(vbase, tokB);
+#pragma unroll
+      for (int mt = 0; mt < KS; ++mt) {
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4_trans(g.chunk_addr(rowB, tokB, 2 * mt + (mi & 1)), a0, a1, a2, a3);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+          MmaOp<T>::run(o[nt][mt], a0, a1, a2, a3, pb[nt][0], pb[nt][1]);
+      }
+    }
+  }
+
+  // Per-warp end state into shared memory: m_s/l_s [GMAX], o_s [GMAX][D+4].
+  __device__ __forceinline__ void store(float *m_s, float *l_s, float *o_s, int lane) {
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        float v = l[nt][j];
+        v += __shfl_xor_sync(0xffffffffu, v, 4);
+        v += __shfl_xor_sync(0xffffffffu, v, 8);
+        v += __shfl_xor_sync(0xffffffffu, v, 16);
+        if (lane < 4) {
+          const int h = nt * 8 + 2 * lane + j;
+          m_s[h] = m[nt][j];
+          l_s[h] = v;
+        }
+      }
+      const int h0 = nt * 8 + 2 * (lane & 3);
+#pragma unroll
+      for (int mt = 0; mt < KS; ++mt) {
+        const int d = mt * 16 + (lane >> 2);
+        o_s[h0 * (D + 4) + d] = o[nt][mt][0];
+        o_s[(h0 + 1) * (D + 4) + d] = o[nt][mt][1];
+        o_s[h0 * (D + 4) + d + 8] = o[nt][mt][2];
+        o_s[(h0 + 1) * (D + 4) + d + 8] = o[nt][mt][3];
+      }
+    }
+  }
+};
+
+// ---------------------------------------------------------------------------
+// CUDA-core fp32 math (any element type; the only path for f32).  Lane
+// (tok = lane % 16, half = lane / 16) forms the dot products of one token
+// with all G query heads over half of D; the halves are summed with one
+// shuffle.  For PV each lane owns D/32 output columns of every head and
+// reads the tile's probabilities from a small shared-memory table.
+template <typename T, int D, int GMAX>
+struct SimtMath {
+  static constexpr int ELT = sizeof(T);
+  static constexpr int CPR = D * ELT / 16;  // 16-byte chunks per row
+  static constexpr int EPC = 16 / ELT;      // elements per chunk
+  static constexpr int DPL = D / 32;        // output columns per lane
+  static constexpr int QP = D + 8;          // q row pitch (floats)
+  float acc[GMAX][DPL];
+  float m[GMAX];
+  float l[GMAX];
+  const float *q_s;
+  float *p_s;
+
+  __device__ __forceinline__ static int qidx(int g, int d) {
+    return g * QP + d + (d >= D / 2 ? 4 : 0);
+  }
+
+  __device__ __forceinline__ void init(const AttnParams &, int, int, int, float *q_smem,
+                                       float *p_smem) {
+    q_s = q_smem;
+    p_s = p_smem;
+#pragma unroll
+    for (int g = 0; g < GMAX; ++g) {
+      m[g] = -CUDART_INF_F;
+      l[g] = 0.f;
+#pragma unroll
+      for (int j = 0; j < DPL; ++j) acc[g][j] = 0.f;
+    }
+  }
+
+  // Cooperative load of the group's queries (all consumer threads).
+  __device__ static void load_q(const AttnParams &p, int s, int kvh, float *q_smem, int tid,
+                                int nthreads) {
+    const T *q = static_cast<const T *>(p.query) +
+                 ((size_t)s * p.num_heads + (size_t)kvh * p.group) * D;
+    for (int i = tid; i < GMAX * D; i += nthreads) {
+      const int g = i / D, d = i % D;
+      q_smem[qidx(g, d)] = g < p.group ? to_float(q[(size_t)g * D + d]) : 0.f;
+    }
+  }
+
+  __device__ __forceinline__ static void widen(const uint4 &c, float (&f)[EPC]) {
+    if constexpr (ELT == 4) {
+      chunk_to_float(c, f);
+    } else if constexpr (sizeof(T) == 2 && std::is_same<T, __nv_bfloat16>::value) {
+      chunk_to_float_bf16(c, f);
+    } else {
+      chunk_to_float_f16(c, f);
+    }
+  }
+
+  // This lane's DPL output columns of token `tok` (row address `row`).
+  __device__ __forceinline__ void load_v(const StageGeom &g, uint32_t row, int tok, int lane,
+                                         float (&v)[DPL]) const {
+    constexpr int BYTES = DPL * ELT;  // 4, 8, 16 or 32
+    const int byte0 = lane * BYTES;
+    if constexpr (BYTES >= 16) {
+#pragma unroll
+      for (int c = 0; c < BYTES / 16; ++c) {
+        uint4 raw;
+        asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                     : "=r"(raw.x), "=r"(raw.y), "=r"(raw.z), "=r"(raw.w)
+                     : "r"(g.chunk_addr(row, tok, byte0 / 16 + c)));
+        float f[EPC];
+        widen(raw, f);
+#pragma unroll
+        for (int e = 0; e < EPC; ++e) v[c * EPC + e] = f[e];
+      }
+    } else {
+      const uint32_t a = g.chunk_addr(row, tok, byte0 / 16) + (uint32_t)(byte0 % 16);
+      uint32_t w[BYTES / 4];
+      if constexpr (BYTES == 8) {
+        asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(w[0]), "=r"(w[1]) : "r"(a));
+      } else {
+        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(w[0]) : "r"(a));
+      }
+#pragma unroll
+      for (int i = 0; i < BYTES / 4; ++i) {
+        if constexpr (ELT == 4) {
+          v[i] = __uint_as_float(w[i]);
+        } else if constexpr (std::is_same<T, __nv_bfloat16>::value) {
+          v[2 * i] = __uint_as_float(w[i] << 16);
+          v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+        } else {
+          const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&w[i]));
+          v[2 * i] = f.x;
+          v[2 * i + 1] = f.y;
+        }
+      }
+    }
+  }
+
+  __device__ __forceinline__ void tile(uint32_t kbase, uint32_t vbase, const StageGeom &g, int tok0,
+                                       int valid, int lane, float scale_log2) {
+    const int tok = lane & 15, half = lane >> 4;
+    float dot[GMAX];
+#pragma unroll
+    for (int gg = 0; gg < GMAX; ++gg) dot[gg] = 0.f;
+    {
+      const uint32_t row = g.row_addr(kbase, tok0 + tok);
+      // Kept rolled: unrolled, every q load is loop-invariant and the
+      // compiler would pin the whole query group in registers.
+#pragma unroll 1
+      for (int c = 0; c < CPR / 2; ++c) {
+        const int chunk = half * (CPR / 2) + c;
+        uint4 raw;
+        asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                     : "=r"(raw.x), "=r"(raw.y), "=r"(raw.z), "=r"(raw.w)
+                     : "r"(g.chunk_addr(row, tok0 + tok, chunk)));
+        float kf[EPC];
+        widen(raw, kf);
+        const int d0 = chunk * EPC;
+#pragma unroll
+        for (int gg = 0; gg < GMAX; ++gg) {
+#pragma unroll
+          for (int e = 0; e < EPC; e += 4) {
+            const float4 qv = *reinterpret_cast<const float4 *>(&q_s[qidx(gg, d0 + e)]);
+            dot[gg] = fmaf(qv.x, kf[e], dot[gg]);
+            dot[gg] = fmaf(qv.y, kf[e + 1], dot[gg]);
+            dot[gg] = fmaf(qv.z, kf[e + 2], dot[gg]);
+            dot[gg] = fmaf(qv.w, kf[e + 3], dot[gg]);
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int gg = 0; gg < GMAX; ++gg) {
+      float x = dot[gg] + __shfl_xor_sync(0xffffffffu, dot[gg], 16);
+      x = tok < valid ? x * scale_log2 : -CUDART_INF_F;
+      float mx = x;
+#pragma unroll
+      for (int off = 1; off < 16; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+      const float mn = fmaxf(m[gg], mx);
+      const float al = exp2f(m[gg] - mn);
+      const float pv = exp2f(x - mn);
+      l[gg] = l[gg] * al + pv;
+      m[gg] = mn;
+#pragma unroll
+      for (int j = 0; j < DPL; ++j) acc[gg][j] *= al;
+      if (half == 0) p_s[tok * GMAX + gg] = pv;
+    }
+    __syncwarp();
+    // ---- PV over the valid tokens only
+    for (int t = 0; t < valid; ++t) {
+      const int tk = tok0 + t;
+      float v[DPL];
+      load_v(g, g.row_addr(vbase, tk), tk, lane, v);
+#pragma unroll
+      for (int gg = 0; gg < GMAX; ++gg) {
+        const float pg = p_s[t * GMAX + gg];
+#pragma unroll
+        for (int j = 0; j < DPL; ++j) acc[gg][j] = fmaf(pg, v[j], acc[gg][j]);
+      }
+    }
+    __syncwarp();
+  }
+
+  __device__ __forceinline__ void store(float *m_s, float *l_s, float *o_s, int lane) {
+#pragma unroll
+    for (int gg = 0; gg < GMAX; ++gg) {
+      float v = l[gg];
+#pragma unroll
+      for (int off = 1; off < 16; off <<= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+      if (lane == 0) {
+        m_s[gg] = m[gg];
+        l_s[gg] = v;
+      }
+#pragma unroll
+      for (int j = 0; j < DPL; ++j) o_s[gg * (D + 4) + lane * DPL + j] = acc[gg][j];
+    }
+  }
+};
+
+// ---------------------------------------------------------------------------
+template <typename T, int D, int NW, int GMAX, class Math, bool SIMT>
+__global__ void __launch_bounds__((NW + 1) * 32, 1)
+    pa_attn_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CUtensorMap tmap_k,
+                   const __grid_constant__ CUtensorMap tmap_v) {
+  constexpr int ELT = sizeof(T);
+  constexpr int ST = NW * kTileTokens;  // tokens per stage
+  constexpr int ROW_BYTES = D * ELT;
+  constexpr int NPANELS = ROW_BYTES / kPanelBytes;
+  constexpr int HALF_BYTES = ST * ROW_BYTES;  // K (or V) bytes of one stage
+  constexpr int NCONS = NW * 32;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int part = blockIdx.x % p.max_parts;
+  const int sk = blockIdx.x / p.max_parts;
+  const int kvh = sk % p.num_kv_heads;
+  const int s = sk / p.num_kv_heads;
+
+  int L = p.seq_lens[s];
+  if (L < 0 || L > p.max_seq_len) {
+    if (threadIdx.x == 0 && part == 0 && kvh == 0) report(p.status, kStatusBadInput);
+    L = L < 0 ? 0 : p.max_seq_len;
+  }
+  const int tok_begin = part * p.range_tokens;
+  if (tok_begin >= L) {
+    if (!p.write_partials && part == 0) {  // V1, empty sequence: zeros
+      T *o = static_cast<T *>(p.out) + ((size_t)s * p.num_heads + (size_t)kvh * p.group) * D;
+      for (int i = threadIdx.x; i < p.group * D; i += blockDim.x) o[i] = from_float<T>(0.f);
+    }
+    return;
+  }
+  const int tok_end = min(tok_begin + p.range_tokens, L);
+  const int n_stages = (tok_end - tok_begin + ST - 1) / ST;
+  const int NST = p.num_stages;
+
+  // ---- shared memory carve-up
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const size_t ring_bytes = (size_t)NST * 2 * HALF_BYTES;
+  const size_t merge_bytes = (size_t)NW * GMAX * (D + 4) * 4 + (size_t)NW * GMAX * 2 * 4;
+  const size_t body = ring_bytes > merge_bytes ? ring_bytes : merge_bytes;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + body);
+  volatile int *flags = reinterpret_cast<volatile int *>(bars + 2 * NST + 1);
+  float *simt_q = reinterpret_cast<float *>(
+      (reinterpret_cast<uintptr_t>(flags) + 16 + 15) & ~uintptr_t(15));  // 16-byte aligned
+  float *simt_p = simt_q + GMAX * (D + 8);
+  const uint32_t ring_u32 = smem_u32(smem);
+  const uint32_t full0 = smem_u32(bars), empty0 = full0 + 8 * NST, never = full0 + 16 * NST;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < NST; ++i) {
+      mbar_init(full0 + 8 * i, 1);
+      mbar_init(empty0 + 8 * i, NW);
+    }
+    mbar_init(never, 1);
+    flags[0] = 0;
+    fence_mbar_init();
+  }
+  if constexpr (SIMT) {
+    if (warp < NW) Math::load_q(p, s, kvh, simt_q, threadIdx.x, NCONS);
+  }
+  __syncthreads();
+
+  const StageGeom geom{p.log2_unit_rows, p.unit_rows - 1, (uint32_t)p.unit_rows * kPanelBytes,
+                       (uint32_t)(NPANELS * p.unit_rows * kPanelBytes)};
+  const uint64_t limit = p.wait_limit_ns;
+
+  if (warp == NW) {
+    // ======================= producer warp =======================
+    if (lane == 0) {
+      prefetch_tmap(&tmap_k);
+      prefetch_tmap(&tmap_v);
+    }
+    const int32_t *bt = p.block_tables + (size_t)s * p.max_blocks_per_seq;
+    const int U = p.unit_rows;
+    const int units_per_stage = ST / U;
+    const int last_page = (tok_end - 1) >> p.log2_block_size;
+    // A window of 64 block-table entries: lane i holds pages win0+i (cur)
+    // and win0+32+i (nxt); it slides by 32 pages when a stage reaches nxt.
+    int win0 = tok_begin >> p.log2_block_size;
+    auto load_entry = [&](int page) -> int { return page <= last_page ? __ldg(bt + page) : -1; };
+    int cur = load_entry(win0 + lane);
+    int nxt = load_entry(win0 + 32 + lane);
+    int issued = 0;
+    bool ok = true;
+    for (int i = 0; i < n_stages; ++i) {
+      const int st = i % NST;
+      if (i >= NST) {
+        bool w = true;
+        if (lane == 0) w = mbar_wait(empty0 + 8 * st, ((i / NST) - 1) & 1, limit, flags);
+        ok = __shfl_sync(0xffffffffu, w, 0);
+        if (!ok) break;
+      }
+      const int stage_tok0 = tok_begin + i * ST;
+      const int n_units = min(units_per_stage, (tok_end - stage_tok0 + U - 1) / U);
+      const int tok = stage_tok0 + lane * U;
+      const int rel = ((lane < n_units ? tok : stage_tok0) >> p.log2_block_size) - win0;
+      const int a = __shfl_sync(0xffffffffu, cur, rel & 31);
+      const int b = __shfl_sync(0xffffffffu, nxt, rel & 31);
+      int y = -1;
+      if (lane < n_units) {
+        const int blk = rel < 32 ? a : b;
+        if ((unsigned)blk >= (unsigned)p.num_blocks) {
+          report(p.status, kStatusBadInput);
+        } else {
+          y = (blk * p.num_kv_heads + kvh) * p.block_size + (tok & (p.block_size - 1));
+        }
+      }
+      const unsigned valid_mask = __ballot_sync(0xffffffffu, y >= 0);
+      if (lane == 0)
+        mbar_arrive_expect_tx(full0 + 8 * st, (uint32_t)__popc(valid_mask) * U * ROW_BYTES * 2);
+      __syncwarp();
+      if (y >= 0) {
+        const uint32_t kdst = ring_u32 + (uint32_t)st * 2 * HALF_BYTES + (uint32_t)lane * geom.unit_bytes;
+        const uint32_t vdst = kdst + HALF_BYTES;
+#pragma unroll
+        for (int pn = 0; pn < NPANELS; ++pn) {
+          tma_load_2d(kdst + pn * geom.panel_bytes, &tmap_k, pn * (kPanelBytes / ELT), y, full0 + 8 * st);
+          tma_load_2d(vdst + pn * geom.panel_bytes, &tmap_v, pn * (kPanelBytes / ELT), y, full0 + 8 * st);
+        }
+      }
+      ++issued;
+      // slide the window once the next stage starts in the nxt half
+      const int next_rel = ((stage_tok0 + ST) >> p.log2_block_size) - win0;
+      if (next_rel >= 32) {
+        cur = nxt;
+        win0 += 32;
+        nxt = load_entry(win0 + 32 + lane);
+      }
+    }
+    if (!ok) {
+      report(p.status, kStatusTimeout);
+      flags[0] = 1;
+    }
+    // Let every copy this CTA started land before the CTA can retire.
+    if (lane == 0) {
+      const int first = issued > NST ? issued - NST : 0;
+      for (int j = first; j < issued; ++j)
+        mbar_wait(full0 + 8 * (j % NST), (j / NST) & 1, kDrainLimitNs, nullptr);
+    }
+    __syncwarp();
+    return;
+  }
+
+  // ======================= consumer warps =======================
+  Math math;
+  math.init(p, s, kvh, lane, simt_q, simt_p + warp * kTileTokens * GMAX);
+  bool ok = true;
+  if (p.debug_flags & kDebugStallConsumers) {
+    // Wait on a barrier that nothing releases: the bound must end it.
+    ok = mbar_wait(never, 0, limit, flags);
+    ok = __all_sync(0xffffffffu, ok);
+  }
+  for (int i = 0; ok && i < n_stages; ++i) {
+    const int st = i % NST;
+    bool w = mbar_wait(full0 + 8 * st, (i / NST) & 1, limit, flags);
+    ok = __all_sync(0xffffffffu, w);
+    if (!ok) break;
+    const int tile_tok0 = tok_begin + i * ST + warp * kTileTokens;
+    const int valid = max(0, min(kTileTokens, tok_end - tile_tok0));
+    if (valid > 0) {
+      const uint32_t kbase = ring_u32 + (uint32_t)st * 2 * HALF_BYTES;
+      math.tile(kbase, kbase + HALF_BYTES, geom, warp * kTileTokens, valid, lane, p.scale_log2);
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty0 + 8 * st);
+  }
+  if (!ok) {
+    if (lane == 0) {
+      report(p.status, kStatusTimeout);
+      flags[0] = 1;
+    }
+  }
+  named_bar_sync(1, NCONS);
+  if (flags[0]) return;
+  pdl_launch_dependents();
+
+  // ---- merge the consumer warps' states (log-sum-exp) and write out
+  float *m_s = reinterpret_cast<float *>(smem);
+  float *l_s = m_s + NW * GMAX;
+  float *o_s = l_s + NW * GMAX;
+  math.store(m_s + warp * GMAX, l_s + warp * GMAX, o_s + (size_t)warp * GMAX * (D + 4), lane);
+  named_bar_sync(1, NCONS);
+
+  const int G = p.group;
+  const size_t head0 = (size_t)s * p.num_heads + (size_t)kvh * G;
+  for (int idx = threadIdx.x; idx < G * D; idx += NCONS) {
+    const int h = idx / D, d = idx % D;
+    float M = -CUDART_INF_F;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) M = fmaxf(M, m_s[w * GMAX + h]);
+    float acc = 0.f, lsum = 0.f;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) {
+      const float f = exp2f(m_s[w * GMAX + h] - M);  // 0 for warps that saw no token
+      acc += f * o_s[((size_t)w * GMAX + h) * (D + 4) + d];
+      lsum += f * l_s[w * GMAX + h];
+    }
+    const float val = acc / lsum;
+    if (p.write_partials) {
+      const size_t row = (head0 + h) * p.max_parts + part;
+      p.tmp_out[row * D + d] = val;
+      if (d == 0) {
+        p.max_logits[row] = M * 0.69314718055994530942f;  // back to natural-log units
+        p.exp_sums[row] = lsum;
+      }
+    } else {
+      static_cast<T *>(p.out)[(head0 + h) * D + d] = from_float<T>(val);
+    }
+  }
+}
+
+template <typename T, int D, int NW, int GMAX, class Math, bool SIMT>
+AttnKernelInfo attn_info() {
+  return AttnKernelInfo{reinterpret_cast<const void *>(&pa_attn_kernel<T, D, NW, GMAX, Math, SIMT>),
+                        NW, NW * kTileTokens, GMAX};
+}
+
+template <typename T>
+AttnKernelInfo select_tensor(int D, int group) {
+  if (group <= 8) {
+    switch (D) {
+      case 64: return attn_info<T, 64, 4, 8, TensorMath<T, 64, 1>, false>();
+      case 128: return attn_info<T, 128, 4, 8, TensorMath<T, 128, 1>, false>();
+      case 256: return attn_info<T, 256, 4, 8, TensorMath<T, 256, 1>, false>();
+    }
+  } else if (group <= 16) {
+    switch (D) {
+      case 64: return attn_info<T, 64, 4, 16, TensorMath<T, 64, 2>, false>();
+      case 128: return attn_info<T, 128, 4, 16, TensorMath<T, 128, 2>, false>();
+      case 256: return attn_info<T, 256, 4, 16, TensorMath<T, 256, 2>, false>();
+    }
+  }
+  return AttnKernelInfo{nullptr, 0, 0, 0};
+}
+
+template <typename T, int D>
+AttnKernelInfo select_simt_d(int group) {
+  constexpr int NW = (D * (int)sizeof(T) >= 1024) ? 2 : 4;
+  if (group <= 4) return attn_info<T, D, NW, 4, SimtMath<T, D, 4>, true>();
+  if (group <= 8) return attn_info<T, D, NW, 8, SimtMath<T, D, 8>, true>();
+  if (group <= 16) return attn_info<T, D, NW, 16, SimtMath<T, D, 16>, true>();
+  return AttnKernelInfo{nullptr, 0, 0, 0};
+}
+
+template <typename T>
+AttnKernelInfo select_simt(int D, int group) {
+  switch (D) {
+    case 64: return select_simt_d<T, 64>(group);
+    case 128: return select_simt_d<T, 128>(group);
+    case 256: return select_simt_d<T, 256>(group);
+  }
+  return AttnKernelInfo{nullptr, 0, 0, 0};
+}
+
+}  // namespace pa

@@ -1,0 +1,84 @@
+// Internal launch parameters shared by the host planner and the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace pa {
+
+constexpr int kTileTokens = 16;     // tokens per warp tile (mma M / N extent)
+constexpr int kPanelBytes = 128;    // TMA box width: one 128-byte swizzle span
+constexpr int kStatusBytes = 256;   // status block at the head of the workspace
+constexpr uint64_t kDefaultWaitLimitNs = 1000000000ull;  // 1 s
+constexpr uint64_t kDrainLimitNs = 1000000000ull;        // drain of own copies
+
+// Parameters of the attention kernel (Phase 1 of V2, or V1).
+struct AttnParams {
+  const void *query;           // [B][H][D]
+  void *out;                   // [B][H][D] (V1) — dtype
+  const int32_t *block_tables; // [B][max_blocks_per_seq]
+  const int32_t *seq_lens;     // [B]
+  float *max_logits;           // [B][H][max_parts]   (V2)
+  float *exp_sums;             // [B][H][max_parts]   (V2)
+  float *tmp_out;              // [B][H][max_parts][D] (V2)
+  int *status;                 // workspace status word
+  int num_seqs, num_heads, num_kv_heads, group;  // group = H / Hkv
+  int block_size, log2_block_size;
+  int unit_rows, log2_unit_rows;  // rows per TMA box: min(block_size, stage tokens)
+  int max_blocks_per_seq, max_seq_len, num_blocks;
+  int range_tokens;   // tokens per CTA: partition_size (V2) or whole sequence (V1)
+  int max_parts;      // CTAs per (seq, kv head)
+  int write_partials; // 1: V2 Phase 1 outputs, 0: V1 final output
+  int num_stages;
+  int debug_flags;
+  float scale_log2;   // scale * log2(e)
+  uint64_t wait_limit_ns;
+};
+
+// Parameters of the Phase 2 (log-sum-exp) reduce kernel.
+struct ReduceParams {
+  void *out;
+  const float *max_logits, *exp_sums, *tmp_out;
+  const int32_t *seq_lens;
+  int *status;
+  int num_seqs, num_heads, head_size, max_parts, partition_size, max_seq_len;
+  int cols_per_cta;  // head_size / grid.z
+};
+
+enum MathKind { kMathSimt = 1, kMathTensor = 2 };
+
+// Static description of one compiled attention kernel.
+struct AttnKernelInfo {
+  const void *fn;     // __global__ function
+  int consumer_warps; // warps computing; one more warp produces (TMA)
+  int stage_tokens;   // consumer_warps * kTileTokens
+  int max_group;      // largest H / Hkv it handles
+};
+
+// Dynamic shared memory the attention kernel needs for `stages` stages.
+inline size_t attn_smem_bytes(int head_size, int elt, int consumer_warps, int max_group,
+                              int stages, bool simt) {
+  size_t stage = (size_t)consumer_warps * kTileTokens * head_size * elt * 2;
+  size_t ring = stage * stages;
+  size_t merge = (size_t)consumer_warps * max_group * (head_size + 4) * 4 +
+                 (size_t)consumer_warps * max_group * 2 * 4;
+  size_t body = ring > merge ? ring : merge;
+  size_t bars = 2 * 8 * (size_t)stages + 8 + 16 + 16;  // full/empty/never-set, flags, pad
+  size_t simt_extra = 0;
+  if (simt) {
+    simt_extra = (size_t)max_group * (head_size + 8) * 4 +                    // q (fp32)
+                 (size_t)consumer_warps * kTileTokens * max_group * 4;       // p tiles
+  }
+  return 1024 /* alignment slack */ + body + bars + simt_extra + 64;
+}
+
+// Kernel tables, one per translation unit (see pa_attn_*.cu).
+AttnKernelInfo attn_kernel_tensor_bf16(int head_size, int group);
+AttnKernelInfo attn_kernel_tensor_f16(int head_size, int group);
+AttnKernelInfo attn_kernel_simt_f32(int head_size, int group);
+AttnKernelInfo attn_kernel_simt_bf16(int head_size, int group);
+AttnKernelInfo attn_kernel_simt_f16(int head_size, int group);
+const void *reduce_kernel(int dtype);
+
+}  // namespace pa

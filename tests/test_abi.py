@@ -1,0 +1,149 @@
+"""libpa's C ABI on the host: the library loads, exports every function the
+header declares, and the host-only entry points (workspace sizing, the V1/V2
+heuristic, status text, argument checks) behave as documented.  CPU only: no
+call here reaches a CUDA API."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import paged_decode_attention_v2_gb300 as pa
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "pa.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import __graft_entry__
+    __graft_entry__.build()
+    return pa.load_library()
+
+
+def header_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pa_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_lists_the_forward_calls():
+    names = header_functions()
+    for n in ("pa_v1_forward", "pa_v2_forward", "pa_forward", "pa_workspace_bytes"):
+        assert n in names
+
+
+def test_library_exports_every_header_function(lib):
+    names = header_functions()
+    assert names, "no declarations parsed"
+    for n in names:
+        assert hasattr(lib, n), f"libpa.so does not export {n}"
+    assert sorted(pa.EXPORTS) == names
+
+
+def test_version_and_status_text(lib):
+    assert pa.pa_version() >= 100
+    for code in range(7):
+        assert pa.pa_status_string(code) and pa.pa_status_string(code) != "unknown status"
+    assert pa.pa_status_string(99) == "unknown status"
+
+
+def test_workspace_layout_and_size(lib):
+    B, H, D, L, P = 3, 32, 128, 100000, 512
+    off = pa.pa_workspace_layout(B, H, D, L, P)
+    parts = -(-L // P)
+    assert parts == 196  # ceil(100000 / 512)
+    assert off[0] == 0 and off[1] == 256
+    assert all(o % 256 == 0 for o in off)
+    stats = B * H * parts * 4
+    assert off[2] - off[1] >= stats and off[2] - off[1] < stats + 256
+    assert off[3] - off[2] == off[2] - off[1]
+    size = pa.pa_workspace_bytes(B, H, D, L, P)
+    assert size >= off[3] + B * H * parts * D * 4 and size % 256 == 0
+    # no partitions: status block only
+    assert pa.pa_workspace_bytes(4, 8, 64, 0, 512) == 256
+    assert pa.pa_workspace_bytes(-1, 8, 64, 10, 512) == 0
+    assert pa.pa_workspace_bytes(1, 8, 64, 10, 0) == 0
+
+
+@pytest.mark.parametrize("args,expect", [
+    ((1, 4, 100000, 512, 152), 1),   # one long sequence: V2 spreads it over the GPU
+    ((8, 4, 8192, 512, 152), 1),     # few (seq, kv head) CTAs: V2
+    ((64, 4, 512, 512, 152), 0),     # every sequence in one partition: V1
+    ((4096, 8, 4096, 512, 152), 0),  # 32K CTAs of short sequences: V1 fills the GPU
+    ((4096, 8, 20000, 512, 152), 1), # long sequences: V2
+    ((1, 1, 0, 512, 152), 0),
+])
+def test_choose_v2(lib, args, expect):
+    assert pa.pa_choose_v2(*args) == expect
+
+
+# ---- argument checks (rejected on the host before any CUDA call) ----------
+
+FAKE = 1 << 20  # aligned, never dereferenced by the host checks
+
+
+def _call(lib, variant=pa.PA_VARIANT_V2, **over):
+    a = dict(out=FAKE, query=FAKE, key_cache=FAKE, value_cache=FAKE, block_tables=FAKE,
+             seq_lens=FAKE, num_seqs=2, num_heads=8, num_kv_heads=2, head_size=128,
+             num_blocks=64, block_size=16, max_blocks_per_seq=8, max_seq_len=128,
+             scale=0.1, partition_size=512, dtype=pa.PA_DTYPE_BF16, workspace=FAKE,
+             workspace_bytes=1 << 30, stream=0)
+    a.update(over)
+    opts = pa.pa_options_t(variant, 0, 0, 0, 0, None)
+    return lib.pa_forward(a["out"], a["query"], a["key_cache"], a["value_cache"],
+                          a["block_tables"], a["seq_lens"], a["num_seqs"], a["num_heads"],
+                          a["num_kv_heads"], a["head_size"], a["num_blocks"], a["block_size"],
+                          a["max_blocks_per_seq"], a["max_seq_len"], a["scale"],
+                          a["partition_size"], a["dtype"], a["workspace"],
+                          a["workspace_bytes"], a["stream"], ctypes.byref(opts))
+
+
+@pytest.mark.parametrize("over,expect", [
+    (dict(out=0), pa.PA_ERR_INVALID_ARG),
+    (dict(query=0), pa.PA_ERR_INVALID_ARG),
+    (dict(key_cache=FAKE + 8), pa.PA_ERR_INVALID_ARG),      # not 16-byte aligned
+    (dict(workspace=FAKE + 16), pa.PA_ERR_INVALID_ARG),     # not 256-byte aligned
+    (dict(block_tables=FAKE + 2), pa.PA_ERR_INVALID_ARG),
+    (dict(num_heads=6, num_kv_heads=4), pa.PA_ERR_INVALID_ARG),
+    (dict(num_heads=64, num_kv_heads=2), pa.PA_ERR_UNSUPPORTED),  # group of 32
+    (dict(head_size=96), pa.PA_ERR_UNSUPPORTED),
+    (dict(block_size=12, max_seq_len=96), pa.PA_ERR_UNSUPPORTED),
+    (dict(block_size=128), pa.PA_ERR_UNSUPPORTED),
+    (dict(partition_size=500), pa.PA_ERR_UNSUPPORTED),
+    (dict(partition_size=16384), pa.PA_ERR_UNSUPPORTED),
+    (dict(partition_size=0), pa.PA_ERR_INVALID_ARG),
+    (dict(dtype=7), pa.PA_ERR_INVALID_ARG),
+    (dict(max_seq_len=129), pa.PA_ERR_INVALID_ARG),         # > max_blocks * block_size
+    (dict(max_seq_len=-1), pa.PA_ERR_INVALID_ARG),
+    (dict(num_seqs=-1), pa.PA_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), pa.PA_ERR_INVALID_ARG),
+    (dict(scale=float("inf")), pa.PA_ERR_INVALID_ARG),
+    (dict(workspace_bytes=255), pa.PA_ERR_WORKSPACE_TOO_SMALL),
+    (dict(num_blocks=1 << 27, num_kv_heads=8, num_heads=8), pa.PA_ERR_UNSUPPORTED),
+])
+def test_argument_errors(lib, over, expect):
+    assert _call(lib, **over) == expect
+
+
+def test_v2_needs_the_partials_workspace(lib):
+    need = pa.pa_workspace_bytes(2, 8, 128, 128, 512)
+    assert _call(lib, workspace_bytes=need - 1) == pa.PA_ERR_WORKSPACE_TOO_SMALL
+    # V1 only needs the status block
+    assert _call(lib, variant=pa.PA_VARIANT_V1, workspace_bytes=255) == \
+        pa.PA_ERR_WORKSPACE_TOO_SMALL
+
+
+def test_empty_batch_is_a_noop(lib):
+    assert _call(lib, num_seqs=0) == pa.PA_OK
+    assert _call(lib, variant=pa.PA_VARIANT_V1, num_seqs=0) == pa.PA_OK
+
+
+def test_bad_variant(lib):
+    assert _call(lib, variant=9) == pa.PA_ERR_INVALID_ARG
+
+
+def test_workspace_init_rejects_bad_buffers(lib):
+    assert lib.pa_workspace_init(0, 256, 0) == pa.PA_ERR_INVALID_ARG
+    assert lib.pa_workspace_init(FAKE, 128, 0) == pa.PA_ERR_INVALID_ARG
+    assert lib.pa_read_device_status(FAKE + 4, 0) == pa.PA_ERR_INVALID_ARG

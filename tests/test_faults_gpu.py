@@ -1,0 +1,95 @@
+"""Device-side failure reporting, exercised without faulting or hanging the
+GPU: bad data is caught by the kernels' own checks and reported through the
+workspace status word; a bounded wait on a barrier that nothing releases runs
+out, reports PA_ERR_DEVICE_TIMEOUT, and the context stays usable."""
+import pytest
+import torch
+
+import paged_decode_attention_v2_gb300 as pa
+import workloads
+from gpu_helpers import DeviceCase, assert_close, reference
+
+pytestmark = pytest.mark.gpu
+
+
+def _case():
+    return workloads.make_case("faults", 81, 4, 16, 2, 128, torch.bfloat16, 16,
+                               [100, 1000, 2500, 7], partition_size=512, extra_blocks=8)
+
+
+@pytest.mark.parametrize("variant", [pa.PA_VARIANT_V1, pa.PA_VARIANT_V2])
+def test_out_of_range_block_id_is_reported(variant):
+    case = _case()
+    dc = DeviceCase(case)
+    bad = dc.bt.clone()
+    bad[1, 10] = case.num_blocks + 5      # past the pool
+    bad[2, 3] = -7                        # negative
+    out = torch.empty_like(dc.q)
+    pa.pa_forward(out, dc.q, dc.kc, dc.vc, bad, dc.sl, case.scale, 512, dc.ws,
+                  max_seq_len=dc.max_seq_len, variant=variant)
+    assert pa.pa_read_device_status(dc.ws) == pa.PA_ERR_DEVICE_BAD_INPUT
+    # the status word was cleared by the read; a good call reports OK
+    out = dc.run(variant=variant)
+    assert_close(out, reference(case), torch.bfloat16)
+
+
+def test_sequence_length_above_bound_is_reported():
+    case = _case()
+    dc = DeviceCase(case)
+    sl = dc.sl.clone()
+    sl[0] = dc.max_seq_len + 1
+    out = torch.empty_like(dc.q)
+    pa.pa_forward(out, dc.q, dc.kc, dc.vc, dc.bt, sl, case.scale, 512, dc.ws,
+                  max_seq_len=dc.max_seq_len, variant=pa.PA_VARIANT_V2)
+    assert pa.pa_read_device_status(dc.ws) == pa.PA_ERR_DEVICE_BAD_INPUT
+    sl[0] = -3
+    pa.pa_forward(out, dc.q, dc.kc, dc.vc, dc.bt, sl, case.scale, 512, dc.ws,
+                  max_seq_len=dc.max_seq_len, variant=pa.PA_VARIANT_V1)
+    assert pa.pa_read_device_status(dc.ws) == pa.PA_ERR_DEVICE_BAD_INPUT
+
+
+@pytest.mark.parametrize("math", [pa.PA_MATH_TENSOR, pa.PA_MATH_SIMT])
+@pytest.mark.parametrize("variant", [pa.PA_VARIANT_V1, pa.PA_VARIANT_V2])
+def test_bounded_wait_runs_out_and_context_survives(variant, math):
+    case = _case()
+    dc = DeviceCase(case)
+    out = torch.zeros_like(dc.q)
+    pa.pa_forward(out, dc.q, dc.kc, dc.vc, dc.bt, dc.sl, case.scale, 512, dc.ws,
+                  max_seq_len=dc.max_seq_len, variant=variant, math=math,
+                  debug_flags=pa.PA_DEBUG_STALL_CONSUMERS, wait_limit_ns=200_000)
+    assert pa.pa_read_device_status(dc.ws) == pa.PA_ERR_DEVICE_TIMEOUT
+    torch.cuda.synchronize()  # the context is still usable
+    out = dc.run(variant=variant, math=math)
+    assert_close(out, reference(case), torch.bfloat16)
+
+
+def test_status_keeps_first_error_until_read():
+    case = _case()
+    dc = DeviceCase(case)
+    out = torch.empty_like(dc.q)
+    pa.pa_forward(out, dc.q, dc.kc, dc.vc, dc.bt, dc.sl, case.scale, 512, dc.ws,
+                  max_seq_len=dc.max_seq_len, variant=pa.PA_VARIANT_V2,
+                  debug_flags=pa.PA_DEBUG_STALL_CONSUMERS, wait_limit_ns=100_000)
+    bad = dc.bt.clone()
+    bad[0, 0] = 1 << 30
+    pa.pa_forward(out, dc.q, dc.kc, dc.vc, bad, dc.sl, case.scale, 512, dc.ws,
+                  max_seq_len=dc.max_seq_len, variant=pa.PA_VARIANT_V2)
+    assert pa.pa_read_device_status(dc.ws) == pa.PA_ERR_DEVICE_TIMEOUT
+    assert pa.pa_read_device_status(dc.ws) == pa.PA_OK
+
+
+def test_host_errors_do_not_launch():
+    case = _case()
+    dc = DeviceCase(case)
+    out = torch.full_like(dc.q, 7.0)
+    with pytest.raises(pa.PAError) as e:
+        pa.pa_forward(out, dc.q, dc.kc, dc.vc, dc.bt, dc.sl, case.scale, 500, dc.ws,
+                      max_seq_len=dc.max_seq_len, variant=pa.PA_VARIANT_V2)
+    assert e.value.status == pa.PA_ERR_UNSUPPORTED
+    small = dc.ws[:1024]
+    with pytest.raises(pa.PAError) as e:
+        pa.pa_forward(out, dc.q, dc.kc, dc.vc, dc.bt, dc.sl, case.scale, 512, small,
+                      max_seq_len=dc.max_seq_len, variant=pa.PA_VARIANT_V2)
+    assert e.value.status == pa.PA_ERR_WORKSPACE_TOO_SMALL
+    torch.cuda.synchronize()
+    assert torch.all(out == 7.0)

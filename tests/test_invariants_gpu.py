@@ -1,0 +1,109 @@
+"""GPU invariants: Phase 1 partials against the oracle's partials, Phase 2
+alone, bit-identical results under a shuffled block pool, V1 == V2 and
+P=256 == P=512 within tolerance, GQA heads == the same heads run as MHA."""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_decode_attention_v2_gb300 as pa
+import workloads
+from gpu_helpers import DeviceCase, assert_close, reference
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("dtype,D,bs,P", [(torch.bfloat16, 128, 16, 512),
+                                          (torch.float32, 64, 16, 256),
+                                          (torch.float16, 256, 32, 256)])
+def test_phase1_partials_match_oracle(dtype, D, bs, P):
+    lens = [1, P - 3, P, P + 1, 3 * P + 100]
+    case = workloads.make_case("partials", 31, len(lens), 16, 2, D, dtype, bs, lens,
+                               partition_size=P, k_mult=3.0)
+    dc = DeviceCase(case)
+    dc.run(variant=pa.PA_VARIANT_V2)
+    ml, es, to = dc.partials()
+    rml, res, rto = oracle.partials(case.query, case.key_cache, case.value_cache,
+                                    case.block_tables, case.seq_lens, case.scale, P)
+    live = ~np.isnan(rml)
+    # max logit: same tolerance as outputs (logits are O(10) here)
+    atol = 1e-4 if dtype == torch.float32 else 2e-2
+    assert np.allclose(ml[live], rml[live], rtol=1e-3, atol=atol)
+    # exp_sums are >= 1 and shift with the max: compare relative
+    rtol = 1e-4 if dtype == torch.float32 else 2e-2
+    assert np.allclose(es[live], res[live], rtol=rtol)
+    assert_close(torch.from_numpy(to[live]), rto[live], dtype, "tmp_out")
+    # Phase 2 alone: the oracle's combine of the GPU's partials equals the
+    # GPU's final output within rounding of the output dtype
+    npt = oracle.num_partitions(case.seq_lens.numpy(), P)
+    comb = oracle.combine(np.nan_to_num(ml), np.nan_to_num(es), np.nan_to_num(to), npt)
+    out = dc.run(variant=pa.PA_VARIANT_V2)
+    assert_close(out, comb, dtype, "phase 2 vs oracle combine of GPU partials")
+
+
+@pytest.mark.parametrize("math", [pa.PA_MATH_TENSOR, pa.PA_MATH_SIMT])
+def test_pool_permutation_is_bit_identical(math):
+    case = workloads.make_case("perm", 41, 6, 32, 4, 128, torch.bfloat16, 16,
+                               [1, 100, 513, 2000, 4097, 777], partition_size=512,
+                               extra_blocks=20)
+    a = DeviceCase(case)
+    b = DeviceCase(workloads.permute_pool(case, 3))
+    for variant in (pa.PA_VARIANT_V1, pa.PA_VARIANT_V2):
+        oa = a.run(variant=variant, math=math)
+        ob = b.run(variant=variant, math=math)
+        assert torch.equal(oa.view(torch.int16), ob.view(torch.int16))
+
+
+def test_v1_equals_v2_and_partition_sizes_agree():
+    case = workloads.config_case("c5_mixed_d256", 512)
+    small = dataclasses.replace(
+        case, query=case.query[:16], block_tables=case.block_tables[:16],
+        seq_lens=case.seq_lens[:16])
+    dc = DeviceCase(small)
+    ref = reference(small)
+    o1 = dc.run(variant=pa.PA_VARIANT_V1)
+    o2 = dc.run(variant=pa.PA_VARIANT_V2, partition_size=512)
+    o3 = dc.run(variant=pa.PA_VARIANT_V2, partition_size=256)
+    for o in (o1, o2, o3):
+        assert_close(o, ref, torch.bfloat16)
+    # the three differ only by rounding: compare to each other at the same bar
+    assert_close(o2, o1.double().cpu().numpy(), torch.bfloat16, "V2 P512 vs V1")
+    assert_close(o3, o2.double().cpu().numpy(), torch.bfloat16, "P256 vs P512")
+
+
+def test_gqa_equals_mha_with_repeated_kv():
+    """Query heads of a GQA group give the same result as MHA with each KV
+    head repeated G times (the kernel's group batching changes nothing)."""
+    G, Hkv = 8, 2
+    case = workloads.make_case("gqa", 51, 3, G * Hkv, Hkv, 128, torch.bfloat16, 16,
+                               [700, 1500, 64], partition_size=512)
+    mha = dataclasses.replace(case, key_cache=case.key_cache.repeat_interleave(G, dim=1),
+                              value_cache=case.value_cache.repeat_interleave(G, dim=1))
+    for variant in (pa.PA_VARIANT_V1, pa.PA_VARIANT_V2):
+        og = DeviceCase(case).run(variant=variant)
+        om = DeviceCase(mha).run(variant=variant)
+        assert_close(og, om.double().cpu().numpy(), torch.bfloat16, "GQA vs MHA")
+
+
+def test_constant_v_gives_v():
+    case = workloads.make_case("constv", 61, 4, 16, 2, 128, torch.bfloat16, 16,
+                               [1, 33, 1000, 5000], partition_size=512, k_mult=4.0)
+    case.value_cache.fill_(0.375)
+    out = DeviceCase(case).run(variant=pa.PA_VARIANT_V2)
+    assert torch.all(out == 0.375)
+
+
+def test_one_hot_logit_selects_one_value():
+    """A key aligned with the query and 30x larger makes one token's weight 1
+    to well within bf16: out == that token's V (after rounding to bf16)."""
+    case = workloads.make_case("onehot", 71, 1, 8, 1, 128, torch.bfloat16, 16, [3000],
+                               partition_size=512)
+    q = case.query[0, 0]
+    blk = int(case.block_tables[0, 1234 // 16])
+    case.query[0, :] = q
+    case.key_cache[blk, 0, 1234 % 16] = (q.float() * 30).to(torch.bfloat16)
+    out = DeviceCase(case).run(variant=pa.PA_VARIANT_V2)
+    v = case.value_cache[blk, 0, 1234 % 16]
+    assert torch.equal(out[0].cpu(), v.expand(8, -1))

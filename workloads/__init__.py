@@ -183,13 +183,24 @@ DESCRIPTIONS = {
 }
 
 
-def config_case(name: str, partition_size: int | None = None) -> DecodeCase:
-    """One of the five named workloads, drawn from seed SEED_BASE + index."""
+def config_case(name: str, partition_size: int | None = None,
+                seed_offset: int = 0) -> DecodeCase:
+    """One of the five named workloads, drawn from seed SEED_BASE + index
+    (+ 1000 * seed_offset: another batch of the same shape, e.g. per rank)."""
     c = dict(CONFIGS[name])
     idx = c.pop("index")
     if partition_size is not None:
         c["partition_size"] = partition_size
-    return make_case(name, SEED_BASE + idx, meta={"config_index": idx}, **c)
+    return make_case(name, SEED_BASE + idx + 1000 * seed_offset,
+                     meta={"config_index": idx}, **c)
+
+
+def sub_batch(case: DecodeCase, num_seqs: int) -> DecodeCase:
+    """The first num_seqs sequences of a case (same cache and pool)."""
+    return replace(case, query=case.query[:num_seqs].contiguous(),
+                   block_tables=case.block_tables[:num_seqs].contiguous(),
+                   seq_lens=case.seq_lens[:num_seqs].contiguous(),
+                   name=f"{case.name}[:{num_seqs}]")
 
 
 def with_partition_size(case: DecodeCase, partition_size: int) -> DecodeCase:
