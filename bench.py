@@ -261,6 +261,12 @@ def time_steps(runner, steps, flush, with_phase=False):
     E = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
     starts, ends = [E() for _ in range(steps)], [E() for _ in range(steps)]
     mids = [E() for _ in range(steps)] if with_phase else None
+    if mids:
+        # torch creates the CUDA event at its first record(); do that here so
+        # the handle handed to the library is live
+        for m in mids:
+            m.record()
+        torch.cuda.synchronize()
     for i in range(steps):
         flush.zero_()
         starts[i].record()

@@ -205,6 +205,9 @@ def pa_forward(out, query, key_cache, value_cache, block_tables, seq_lens, scale
     ev = 0
     if phase1_event is not None:
         ev = phase1_event.cuda_event if hasattr(phase1_event, "cuda_event") else int(phase1_event)
+        if not ev:
+            raise ValueError("phase1_event has no CUDA event yet (torch creates it at the "
+                             "first record(); record it once before passing it)")
     opts = pa_options_t(variant, math, num_stages, debug_flags, wait_limit_ns, ev)
     _check(load_library().pa_forward(*_fwd_args(
         out, query, key_cache, value_cache, block_tables, seq_lens, scale, partition_size,

@@ -85,7 +85,7 @@ def test_partition_sizes(P):
     assert_close(out, ref, torch.bfloat16, f"P={P}")
 
 
-@pytest.mark.parametrize("stages", [2, 3, 4, 6, 8])
+@pytest.mark.parametrize("stages", [2, 3, 4, 6])
 def test_pipeline_depths(stages):
     case = workloads.make_case("stages", 5, 4, 32, 4, 128, torch.bfloat16, 16,
                                [3000, 517, 4096, 77], partition_size=512)
@@ -94,6 +94,16 @@ def test_pipeline_depths(stages):
     for variant in (pa.PA_VARIANT_V1, pa.PA_VARIANT_V2):
         out = dc.run(variant=variant, num_stages=stages)
         assert_close(out, ref, torch.bfloat16, f"stages={stages} v{variant}")
+
+
+def test_stages_beyond_shared_memory_are_rejected():
+    """8 stages of 32 KB exceed the 227 KB a CTA may use: refused on the host."""
+    case = workloads.make_case("stages8", 6, 1, 8, 1, 128, torch.bfloat16, 16, [1000],
+                               partition_size=512)
+    dc = DeviceCase(case)
+    with pytest.raises(pa.PAError) as e:
+        dc.run(variant=pa.PA_VARIANT_V2, num_stages=8)
+    assert e.value.status == pa.PA_ERR_UNSUPPORTED
 
 
 def test_empty_sequences_give_zeros():
