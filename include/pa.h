@@ -152,6 +152,37 @@ pa_status_t pa_forward(void *out, const void *query, const void *key_cache,
                        void *workspace, size_t workspace_bytes, void *stream,
                        const pa_options_t *opts);
 
+/* V2 for callers that cannot allocate device memory, for example a plug-in
+ * whose host framework owns all device memory and forbids cudaMalloc while
+ * it serves a request, or a serving loop that must not pay cudaMalloc's
+ * implicit synchronisation.  The paged_attention_v2 pages have no
+ * counterpart: this entry point exists only for such callers.
+ *
+ * Same arguments as pa_v2_forward, minus the workspace.  V2's scratch comes
+ * from a fixed 32 MiB array in device memory owned by the library.  Every
+ * GPU that loads the library holds the array until the process exits.
+ * Requests whose pa_workspace_bytes(...) exceeds 32 MiB return
+ * PA_ERR_WORKSPACE_TOO_SMALL.  The call allocates nothing and calls no
+ * allocating routine.
+ *
+ * The first call on a device looks up the array's device address (with that
+ * device current); make that first call before any stream capture.  All
+ * calls on a device share the one array and each overwrites what the last
+ * left there, so calls whose kernels overlap on the GPU race: serialise
+ * them.  Device-detected data errors land in the shared array's status word,
+ * which each call clears; callers that need pa_read_device_status use
+ * pa_v2_forward with their own workspace. */
+pa_status_t pa_v2_forward_noalloc(void *out, const void *query,
+                                  const void *key_cache,
+                                  const void *value_cache,
+                                  const int32_t *block_tables,
+                                  const int32_t *seq_lens, int num_seqs,
+                                  int num_heads, int num_kv_heads,
+                                  int head_size, int num_blocks,
+                                  int block_size, int max_blocks_per_seq,
+                                  int max_seq_len, float scale,
+                                  int partition_size, int dtype, void *stream);
+
 /* Host heuristic: 1 if V2 should serve this batch on a GPU with sm_count
  * SMs, 0 for V1.  V1 when every sequence fits in one partition; otherwise V2
  * unless the batch alone fills the GPU several times over with short

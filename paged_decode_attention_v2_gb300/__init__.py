@@ -42,7 +42,7 @@ _DTYPES = {torch.float32: PA_DTYPE_F32, torch.bfloat16: PA_DTYPE_BF16,
 EXPORTS = ("pa_workspace_bytes", "pa_workspace_layout", "pa_workspace_init",
            "pa_v1_forward", "pa_v2_forward", "pa_forward", "pa_choose_v2",
            "pa_read_device_status", "pa_status_string", "pa_last_cuda_error",
-           "pa_version")
+           "pa_version", "pa_v2_forward_noalloc")
 
 
 class PAError(RuntimeError):
@@ -87,6 +87,8 @@ def load_library(path: str = LIB_PATH):
             f = getattr(lib, name)
             f.restype = ci
             f.argtypes = _FWD_ARGS
+        lib.pa_v2_forward_noalloc.restype = ci
+        lib.pa_v2_forward_noalloc.argtypes = _FWD_ARGS[:17] + [vp]
         lib.pa_forward.restype = ci
         lib.pa_forward.argtypes = _FWD_ARGS + [ctypes.POINTER(pa_options_t)]
         lib.pa_choose_v2.restype = ci
@@ -194,6 +196,17 @@ def pa_v2_forward(out, query, key_cache, value_cache, block_tables, seq_lens, sc
     _check(load_library().pa_v2_forward(*_fwd_args(
         out, query, key_cache, value_cache, block_tables, seq_lens, scale, partition_size,
         workspace, max_seq_len, stream)), "pa_v2_forward")
+
+
+def pa_v2_forward_noalloc(out, query, key_cache, value_cache, block_tables, seq_lens, scale,
+                          partition_size, max_seq_len=None, stream=None) -> None:
+    """V2 without a caller workspace, for callers that cannot allocate device
+    memory: scratch comes from the library's fixed 32 MiB device array (one
+    per GPU, shared by all calls; overlapping calls race)."""
+    args = _fwd_args(out, query, key_cache, value_cache, block_tables, seq_lens, scale,
+                     partition_size, torch.empty(0, dtype=torch.uint8), max_seq_len, stream)
+    _check(load_library().pa_v2_forward_noalloc(*args[:17], args[19]),
+           "pa_v2_forward_noalloc")
 
 
 def pa_forward(out, query, key_cache, value_cache, block_tables, seq_lens, scale,
