@@ -250,9 +250,26 @@ class Runner:
             raise RuntimeError(f"device status {st}: {self.pa.pa_status_string(st)}")
 
 
+class L2Flush:
+    """Evicts the workload from L2 before a timed step: writes a buffer of
+    twice the L2 size, then reads a second one, so that the dirty lines of the
+    write are written back here (outside the timed events) and not during
+    the timed kernel."""
+
+    def __init__(self, device):
+        l2 = torch.cuda.get_device_properties(device).L2_cache_size
+        n = max(2 * l2, 256 << 20) // 4
+        self.w = torch.empty(n, dtype=torch.float32, device=device)
+        self.r = torch.zeros(n, dtype=torch.float32, device=device)
+        self.sink = torch.empty((), dtype=torch.float32, device=device)
+
+    def zero_(self):
+        self.w.zero_()
+        torch.sum(self.r, dim=0, out=self.sink)
+
+
 def l2_flush_buffer(device):
-    l2 = torch.cuda.get_device_properties(device).L2_cache_size
-    return torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device=device)
+    return L2Flush(device)
 
 
 def time_steps(runner, steps, flush, with_phase=False):
@@ -397,7 +414,7 @@ def run_ours(args):
             "mean_seq_len": round(float(case.seq_lens.double().mean()), 1),
             "kv_bytes_per_step": case.kv_bytes(),
             "variant": "v2" if runner.is_v2 else "v1", "math": args.math,
-            "l2": "flushed before every timed step (write of 2x L2, outside the events)",
+            "l2": "flushed before every timed step (write then read of 2x L2 each, outside the events)",
             "parallelism": f"dp{world} (independent batches per GPU)",
         },
         "tokens_per_s": round(seqs_all * args.steps / total_s_max, 1),

@@ -158,7 +158,7 @@ int max_parts_of(int max_seq_len, int partition_size) {
   return (max_seq_len + partition_size - 1) / partition_size;
 }
 
-constexpr int kMaxReduceParts = 40000;  // Phase 2 keeps one weight per partition in smem
+constexpr int kMaxReduceParts = 1 << 20;  // bound on partitions per sequence
 
 // Checks that need no device.  need_v2: the workspace must hold the partials.
 pa_status_t check_args(const Call &c, bool need_v2) {
@@ -211,10 +211,12 @@ AttnKernelInfo pick_kernel(int math, int dtype, int head_size, int group) {
   return AttnKernelInfo{nullptr, 0, 0, 0};
 }
 
-// Default pipeline depth: about 96 KB of K+V stages per CTA, so that two
-// CTAs share an SM and each keeps 64 KB or more of loads in flight.
+// Default pipeline depth: about 64 KB of K+V stages per CTA.  Measured on
+// GB300, three CTAs per SM with two 32 KB stages each stream faster than
+// fewer CTAs with deeper rings: the other CTAs on the SM cover each CTA's
+// start-up and epilogue.
 int default_stages(size_t stage_bytes) {
-  int n = (int)((96 * 1024) / stage_bytes);
+  int n = (int)((64 * 1024) / stage_bytes);
   return n < 2 ? 2 : (n > 8 ? 8 : n);
 }
 
@@ -327,19 +329,24 @@ pa_status_t launch(const Call &c, bool v2, const pa_options_t &opt) {
   r.max_parts = p.max_parts;
   r.partition_size = c.partition_size;
   r.max_seq_len = c.max_seq_len;
+  // Warps per (sequence, head): enough that each warp's chain of dependent
+  // tmp_out loads stays short; then split columns over CTAs until the grid
+  // covers the GPU twice.
   const long long pairs = (long long)c.num_seqs * c.num_heads;
-  const int dsplit = pairs < 2LL * dev->sm_count ? c.head_size / 32 : 1;
+  const int wph = p.max_parts <= 16 ? 1 : p.max_parts <= 32 ? 2 : p.max_parts <= 64 ? 4 : 8;
+  const long long groups = 8 / wph;
+  const long long ctas = (pairs + groups - 1) / groups;
+  int dsplit = 1;
+  while (ctas * dsplit < 2LL * dev->sm_count && c.head_size / (dsplit * 2) >= 32) dsplit *= 2;
   r.cols_per_cta = c.head_size / dsplit;
+  r.warps_per_head = wph;
   const void *rfn = reduce_kernel(c.dtype);
-  const size_t rsmem = 256 * 16 + (size_t)p.max_parts * 4;
-  st = ensure_smem(rfn, rsmem);
-  if (st != PA_OK) return st;
   if (pairs == 0) return PA_OK;
   cudaLaunchConfig_t cfg;
   memset(&cfg, 0, sizeof cfg);
-  cfg.gridDim = dim3((unsigned)pairs, (unsigned)dsplit, 1);
+  cfg.gridDim = dim3((unsigned)ctas, (unsigned)dsplit, 1);
   cfg.blockDim = dim3(256, 1, 1);
-  cfg.dynamicSmemBytes = rsmem;
+  cfg.dynamicSmemBytes = 0;
   cfg.stream = c.stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

@@ -605,19 +605,27 @@ AttnKernelInfo attn_info() {
                         NW, NW * kTileTokens, GMAX};
 }
 
+// Consumer warps per CTA: a stage is NW x 16 tokens; keep it at 32 KB of K+V
+// for rows of 256 bytes or more (4, 2 or 1 warps), so that two stages leave
+// room for three CTAs on an SM.
+template <typename T, int D>
+constexpr int consumer_warps() {
+  return D * (int)sizeof(T) <= 256 ? 4 : (D * (int)sizeof(T) <= 512 ? 2 : 1);
+}
+
 template <typename T>
 AttnKernelInfo select_tensor(int D, int group) {
   if (group <= 8) {
     switch (D) {
-      case 64: return attn_info<T, 64, 4, 8, TensorMath<T, 64, 1>, false>();
-      case 128: return attn_info<T, 128, 4, 8, TensorMath<T, 128, 1>, false>();
-      case 256: return attn_info<T, 256, 4, 8, TensorMath<T, 256, 1>, false>();
+      case 64: return attn_info<T, 64, consumer_warps<T, 64>(), 8, TensorMath<T, 64, 1>, false>();
+      case 128: return attn_info<T, 128, consumer_warps<T, 128>(), 8, TensorMath<T, 128, 1>, false>();
+      case 256: return attn_info<T, 256, consumer_warps<T, 256>(), 8, TensorMath<T, 256, 1>, false>();
     }
   } else if (group <= 16) {
     switch (D) {
-      case 64: return attn_info<T, 64, 4, 16, TensorMath<T, 64, 2>, false>();
-      case 128: return attn_info<T, 128, 4, 16, TensorMath<T, 128, 2>, false>();
-      case 256: return attn_info<T, 256, 4, 16, TensorMath<T, 256, 2>, false>();
+      case 64: return attn_info<T, 64, consumer_warps<T, 64>(), 16, TensorMath<T, 64, 2>, false>();
+      case 128: return attn_info<T, 128, consumer_warps<T, 128>(), 16, TensorMath<T, 128, 2>, false>();
+      case 256: return attn_info<T, 256, consumer_warps<T, 256>(), 16, TensorMath<T, 256, 2>, false>();
     }
   }
   return AttnKernelInfo{nullptr, 0, 0, 0};
@@ -625,7 +633,7 @@ AttnKernelInfo select_tensor(int D, int group) {
 
 template <typename T, int D>
 AttnKernelInfo select_simt_d(int group) {
-  constexpr int NW = (D * (int)sizeof(T) >= 1024) ? 2 : 4;
+  constexpr int NW = consumer_warps<T, D>();
   if (group <= 4) return attn_info<T, D, NW, 4, SimtMath<T, D, 4>, true>();
   if (group <= 8) return attn_info<T, D, NW, 8, SimtMath<T, D, 8>, true>();
   if (group <= 16) return attn_info<T, D, NW, 16, SimtMath<T, D, 16>, true>();

@@ -43,7 +43,8 @@ struct ReduceParams {
   const int32_t *seq_lens;
   int *status;
   int num_seqs, num_heads, head_size, max_parts, partition_size, max_seq_len;
-  int cols_per_cta;  // head_size / grid.z
+  int cols_per_cta;    // head_size / gridDim.y
+  int warps_per_head;  // 1, 2, 4 or 8 warps share one (sequence, head)
 };
 
 enum MathKind { kMathSimt = 1, kMathTensor = 2 };

@@ -4,10 +4,17 @@
 //   M     = max_p max_logits[p]
 //   r_p   = exp(max_logits[p] - M) * exp_sums[p]
 //   out   = sum_p (r_p / sum_p' r_p') * tmp_out[p]
-// One CTA per (sequence, query head) x column slice of the head.  The weights
-// r_p go to shared memory once; the weighted sum of the tmp_out rows is
-// spread over all threads with 16-byte loads, several partitions in flight
-// per thread, then folded across thread rows in shared memory.
+//
+// A group of `wph` warps (1, 2, 4 or 8) serves one (sequence, query head) and
+// a slice of `cols_per_cta` columns of it; a 256-thread CTA holds 8 / wph such
+// groups.  Every warp of a group finds M and sum r_p over all partitions by
+// itself (warp shuffles, no block barrier), then takes every wph-th
+// partition and accumulates r_p * tmp_out[p] over its columns with 16-byte
+// loads, four partitions in flight.  With wph > 1 the warps' partial sums
+// meet once in shared memory.  One warp per head suits batches whose
+// sequences span few partitions; long sequences split their partitions over
+// up to 8 warps (and their columns over several CTAs) to keep the load chain
+// short.
 #include <math_constants.h>
 
 #include "pa_device.cuh"
@@ -16,28 +23,6 @@ namespace pa {
 
 constexpr int kReduceThreads = 256;
 
-__device__ __forceinline__ float block_max(float v, float *scratch) {
-  for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
-  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (lane == 0) scratch[w] = v;
-  __syncthreads();
-  v = lane < (int)(blockDim.x >> 5) ? scratch[lane] : -CUDART_INF_F;
-  for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
-  __syncthreads();
-  return v;
-}
-
-__device__ __forceinline__ float block_sum(float v, float *scratch) {
-  for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (lane == 0) scratch[w] = v;
-  __syncthreads();
-  v = lane < (int)(blockDim.x >> 5) ? scratch[lane] : 0.f;
-  for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-  __syncthreads();
-  return v;
-}
-
 template <typename OutT>
 __global__ void __launch_bounds__(kReduceThreads)
     pa_v2_reduce_kernel(const __grid_constant__ ReduceParams p) {
@@ -45,86 +30,128 @@ __global__ void __launch_bounds__(kReduceThreads)
   // has finished; wait here until all of its results are visible.
   pdl_wait_primary();
 
-  const int h = blockIdx.x % p.num_heads, s = blockIdx.x / p.num_heads;
+  __shared__ float4 part_sum[kReduceThreads / 32][64];  // [warp][<= 256 cols / 4]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int wph = p.warps_per_head;
+  const int groups = (kReduceThreads / 32) / wph;
+  const int g = warp / wph, wig = warp % wph;  // group in CTA, warp in group
+  const long long pair = (long long)blockIdx.x * groups + g;
+  const bool live = pair < (long long)p.num_seqs * p.num_heads;
+  const int s = live ? (int)(pair / p.num_heads) : 0;
+  const int h = live ? (int)(pair % p.num_heads) : 0;
   const int D = p.head_size;
-  const int col0 = blockIdx.y * p.cols_per_cta;
   const int ncols = p.cols_per_cta;
-  int L = p.seq_lens[s];
-  L = L < 0 ? 0 : (L > p.max_seq_len ? p.max_seq_len : L);  // Phase 1 reported it
-  const int np = (L + p.partition_size - 1) / p.partition_size;
-  OutT *out = static_cast<OutT *>(p.out) + ((size_t)s * p.num_heads + h) * D + col0;
-  if (np == 0) {
-    for (int c = threadIdx.x; c < ncols; c += blockDim.x) out[c] = from_float<OutT>(0.f);
-    return;
+  const int col0 = blockIdx.y * ncols;
+
+  int np = 0;
+  if (live) {
+    int L = p.seq_lens[s];
+    L = L < 0 ? 0 : (L > p.max_seq_len ? p.max_seq_len : L);  // Phase 1 reported it
+    np = (L + p.partition_size - 1) / p.partition_size;
   }
-
-  extern __shared__ float4 red_smem[];                       // [256] row partial sums
-  float *w_s = reinterpret_cast<float *>(red_smem + kReduceThreads);  // [max_parts]
-  __shared__ float scratch[32];
-
+  OutT *out = static_cast<OutT *>(p.out) + ((size_t)s * p.num_heads + h) * D + col0;
   const size_t row0 = ((size_t)s * p.num_heads + h) * p.max_parts;
   const float *ml = p.max_logits + row0;
   const float *es = p.exp_sums + row0;
 
+  // ---- M and the normaliser, per warp
   float mx = -CUDART_INF_F;
-  for (int i = threadIdx.x; i < np; i += blockDim.x) mx = fmaxf(mx, ml[i]);
-  mx = block_max(mx, scratch);
+  for (int i = lane; i < np; i += 32) mx = fmaxf(mx, __ldcg(ml + i));
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
   float wsum = 0.f;
-  for (int i = threadIdx.x; i < np; i += blockDim.x) {
-    const float w = expf(ml[i] - mx) * es[i];
-    w_s[i] = w;
-    wsum += w;
-  }
-  wsum = block_sum(wsum, scratch);  // (ends with __syncthreads: w_s is visible)
+  for (int i = lane; i < np; i += 32) wsum += expf(__ldcg(ml + i) - mx) * __ldcg(es + i);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, off);
 
-  const int tpr = ncols / 4;                  // threads per tmp_out row (float4 each)
-  const int rows_par = kReduceThreads / tpr;  // rows in flight
-  const int c4 = threadIdx.x % tpr, r0 = threadIdx.x / tpr;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  const float *tmp = p.tmp_out + row0 * D + col0 + 4 * c4;
-  int i = r0;
-  for (; i + 3 * rows_par < np; i += 4 * rows_par) {
-    float4 v[4];
+  // ---- weighted sum over this warp's partitions
+  // lanes: `lpr` lanes per row (one float4 each, several if ncols > 128),
+  // `rpi` rows per warp iteration
+  const int c4 = ncols / 4;                // float4s per row
+  const int lpr = c4 < 32 ? c4 : 32;       // lanes per row
+  const int rpi = 32 / lpr;                // rows per iteration
+  const int per_lane = c4 / lpr;           // float4s per lane (1 or 2)
+  const int sub = lane / lpr, cl = lane % lpr;
+  float4 acc[2] = {make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
+  const float *tmp = p.tmp_out + row0 * D + col0 + 4 * cl;
+  const int stride = wph * rpi;
+  int i = wig * rpi + sub;
+  for (; i + 3 * stride < np; i += 4 * stride) {
+    float4 v[4][2];
     float w[4];
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
-      v[u] = __ldcg(reinterpret_cast<const float4 *>(tmp + (size_t)(i + u * rows_par) * D));
-      w[u] = w_s[i + u * rows_par];
+      const int r = i + u * stride;
+      w[u] = expf(__ldcg(ml + r) - mx) * __ldcg(es + r);
+#pragma unroll
+      for (int k = 0; k < 2; ++k)
+        if (k < per_lane)
+          v[u][k] = __ldcg(reinterpret_cast<const float4 *>(tmp + (size_t)r * D + 4 * lpr * k));
     }
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      acc.x = fmaf(w[u], v[u].x, acc.x);
-      acc.y = fmaf(w[u], v[u].y, acc.y);
-      acc.z = fmaf(w[u], v[u].z, acc.z);
-      acc.w = fmaf(w[u], v[u].w, acc.w);
+    for (int u = 0; u < 4; ++u)
+#pragma unroll
+      for (int k = 0; k < 2; ++k)
+        if (k < per_lane) {
+          acc[k].x = fmaf(w[u], v[u][k].x, acc[k].x);
+          acc[k].y = fmaf(w[u], v[u][k].y, acc[k].y);
+          acc[k].z = fmaf(w[u], v[u][k].z, acc[k].z);
+          acc[k].w = fmaf(w[u], v[u][k].w, acc[k].w);
+        }
+  }
+  for (; i < np; i += stride) {
+    const float w = expf(__ldcg(ml + i) - mx) * __ldcg(es + i);
+#pragma unroll
+    for (int k = 0; k < 2; ++k)
+      if (k < per_lane) {
+        const float4 v = __ldcg(reinterpret_cast<const float4 *>(tmp + (size_t)i * D + 4 * lpr * k));
+        acc[k].x = fmaf(w, v.x, acc[k].x);
+        acc[k].y = fmaf(w, v.y, acc[k].y);
+        acc[k].z = fmaf(w, v.z, acc[k].z);
+        acc[k].w = fmaf(w, v.w, acc[k].w);
+      }
+  }
+  // fold the rows handled by different lane groups of the warp
+  for (int off = lpr; off < 32; off <<= 1)
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      acc[k].x += __shfl_xor_sync(0xffffffffu, acc[k].x, off);
+      acc[k].y += __shfl_xor_sync(0xffffffffu, acc[k].y, off);
+      acc[k].z += __shfl_xor_sync(0xffffffffu, acc[k].z, off);
+      acc[k].w += __shfl_xor_sync(0xffffffffu, acc[k].w, off);
+    }
+  if (wph > 1) {
+    if (sub == 0) {
+#pragma unroll
+      for (int k = 0; k < 2; ++k)
+        if (k < per_lane) part_sum[warp][cl + lpr * k] = acc[k];
+    }
+    __syncthreads();
+    if (wig != 0) return;
+    if (sub == 0) {
+#pragma unroll
+      for (int k = 0; k < 2; ++k)
+        if (k < per_lane)
+          for (int w2 = 1; w2 < wph; ++w2) {
+            const float4 t = part_sum[warp + w2][cl + lpr * k];
+            acc[k].x += t.x;
+            acc[k].y += t.y;
+            acc[k].z += t.z;
+            acc[k].w += t.w;
+          }
     }
   }
-  for (; i < np; i += rows_par) {
-    const float4 v = __ldcg(reinterpret_cast<const float4 *>(tmp + (size_t)i * D));
-    const float w = w_s[i];
-    acc.x = fmaf(w, v.x, acc.x);
-    acc.y = fmaf(w, v.y, acc.y);
-    acc.z = fmaf(w, v.z, acc.z);
-    acc.w = fmaf(w, v.w, acc.w);
-  }
-  red_smem[threadIdx.x] = acc;
-  __syncthreads();
-  if (threadIdx.x < tpr) {
-    float4 t = red_smem[threadIdx.x];
-    for (int r = 1; r < rows_par; ++r) {
-      const float4 u = red_smem[r * tpr + threadIdx.x];
-      t.x += u.x;
-      t.y += u.y;
-      t.z += u.z;
-      t.w += u.w;
+  if (!live || sub != 0) return;
+  const float inv = np > 0 ? 1.f / wsum : 0.f;  // np == 0: empty sequence -> zeros
+#pragma unroll
+  for (int k = 0; k < 2; ++k)
+    if (k < per_lane) {
+      OutT *o = out + 4 * (cl + lpr * k);
+      o[0] = from_float<OutT>(acc[k].x * inv);
+      o[1] = from_float<OutT>(acc[k].y * inv);
+      o[2] = from_float<OutT>(acc[k].z * inv);
+      o[3] = from_float<OutT>(acc[k].w * inv);
     }
-    const float inv = 1.f / wsum;
-    OutT *o = out + 4 * threadIdx.x;
-    o[0] = from_float<OutT>(t.x * inv);
-    o[1] = from_float<OutT>(t.y * inv);
-    o[2] = from_float<OutT>(t.z * inv);
-    o[3] = from_float<OutT>(t.w * inv);
-  }
 }
 
 const void *reduce_kernel(int dtype) {
