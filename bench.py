@@ -58,6 +58,7 @@ def parse_args(argv=None):
     ap.add_argument("--variant", choices=["auto", "v1", "v2"], default="auto")
     ap.add_argument("--math", choices=["auto", "tensor", "simt"], default="auto")
     ap.add_argument("--stages", type=int, default=0)
+    ap.add_argument("--ctas-per-sm", type=int, default=0)
     ap.add_argument("--partition-size", type=int, default=0)
     ap.add_argument("--no-secondary", action="store_true",
                     help="skip the extra long-context measurement")
@@ -208,7 +209,7 @@ def algorithmic_bytes(case, v2: bool) -> dict:
 class Runner:
     """A workload resident on the GPU plus the call that runs one step."""
 
-    def __init__(self, case, device, variant, math, stages):
+    def __init__(self, case, device, variant, math, stages, ctas_per_sm=0):
         import paged_decode_attention_v2_gb300 as pa
         self.pa = pa
         self.case = case
@@ -225,6 +226,7 @@ class Runner:
         self.math = {"auto": pa.PA_MATH_AUTO, "tensor": pa.PA_MATH_TENSOR,
                      "simt": pa.PA_MATH_SIMT}[math]
         self.stages = stages
+        self.ctas_per_sm = ctas_per_sm
         self.ws = pa.alloc_workspace(case.num_seqs, case.num_heads, case.head_size,
                                      self.max_seq_len, case.partition_size, device=device)
         sm = torch.cuda.get_device_properties(device).multi_processor_count
@@ -242,7 +244,8 @@ class Runner:
                            sl if sl is not None else self.sl,
                            self.case.scale, self.case.partition_size, self.ws,
                            max_seq_len=self.max_seq_len, variant=self.variant, math=self.math,
-                           num_stages=self.stages, phase1_event=phase1_event)
+                           num_stages=self.stages, phase1_event=phase1_event,
+                           ctas_per_sm=self.ctas_per_sm)
 
     def check_status(self):
         st = self.pa.pa_read_device_status(self.ws)
@@ -356,7 +359,7 @@ def run_ours(args):
 
     P = args.partition_size or None
     case = workloads.config_case(args.workload, P, seed_offset=rank)
-    runner = Runner(case, device, args.variant, args.math, args.stages)
+    runner = Runner(case, device, args.variant, args.math, args.stages, args.ctas_per_sm)
     flush = l2_flush_buffer(device)
     for _ in range(args.warmup):
         runner.step()

@@ -83,6 +83,8 @@ typedef struct {
   void *phase1_event;     /* cudaEvent_t or NULL: for V2, recorded on the
                              stream between the Phase 1 and Phase 2 kernels
                              (lets a caller time the phases with events)   */
+  int32_t ctas_per_sm;    /* persistent CTAs per SM, 0 = as many as fit     */
+  int32_t reserved;       /* 0                                              */
 } pa_options_t;
 
 /* Debug: every consumer warp waits on a barrier that nothing ever releases,
@@ -94,7 +96,7 @@ typedef struct {
 /* Bytes of workspace that pa_v2_forward needs (V1 needs only the 256-byte
  * status block; so does V2 for max_seq_len == 0).  Layout, each part
  * 256-byte aligned, in this order:
- *   status      int32 (first 4 bytes of a 256-byte block)
+ *   status      int32 status word + work-queue counters (a 256-byte block)
  *   max_logits  f32 [num_seqs][num_heads][max_parts]   Phase 1 max logit
  *   exp_sums    f32 [num_seqs][num_heads][max_parts]   sum exp(logit - max)
  *   tmp_out     f32 [num_seqs][num_heads][max_parts][head_size]  normalised
@@ -109,8 +111,10 @@ pa_status_t pa_workspace_layout(int num_seqs, int num_heads, int head_size,
                                 int max_seq_len, int partition_size,
                                 size_t offsets[4]);
 
-/* Zero the status word of a new workspace (enqueued on `stream`).  Call once
- * after allocating it; the kernels only ever write a nonzero code. */
+/* Zero the status block of a new workspace (enqueued on `stream`).  Call
+ * once after allocating it.  The block holds the status word, which kernels
+ * only ever set to a nonzero code, and the work-queue counters of the
+ * attention kernel, which every launch leaves at zero when it finishes. */
 pa_status_t pa_workspace_init(void *workspace, size_t workspace_bytes,
                               void *stream);
 

@@ -54,7 +54,8 @@ class PAError(RuntimeError):
 class pa_options_t(ctypes.Structure):
     _fields_ = [("variant", ctypes.c_int32), ("math", ctypes.c_int32),
                 ("num_stages", ctypes.c_int32), ("debug_flags", ctypes.c_int32),
-                ("wait_limit_ns", ctypes.c_uint64), ("phase1_event", ctypes.c_void_p)]
+                ("wait_limit_ns", ctypes.c_uint64), ("phase1_event", ctypes.c_void_p),
+                ("ctas_per_sm", ctypes.c_int32), ("reserved", ctypes.c_int32)]
 
 
 _lib = None
@@ -212,7 +213,7 @@ def pa_v2_forward_noalloc(out, query, key_cache, value_cache, block_tables, seq_
 def pa_forward(out, query, key_cache, value_cache, block_tables, seq_lens, scale,
                partition_size, workspace, max_seq_len=None, stream=None, variant=PA_VARIANT_AUTO,
                math=PA_MATH_AUTO, num_stages=0, debug_flags=0, wait_limit_ns=0,
-               phase1_event=None) -> None:
+               phase1_event=None, ctas_per_sm=0) -> None:
     """V1 or V2 chosen by pa_choose_v2, or forced through the options.
     ``phase1_event`` (a torch.cuda.Event) is recorded between V2's two kernels."""
     ev = 0
@@ -221,7 +222,7 @@ def pa_forward(out, query, key_cache, value_cache, block_tables, seq_lens, scale
         if not ev:
             raise ValueError("phase1_event has no CUDA event yet (torch creates it at the "
                              "first record(); record it once before passing it)")
-    opts = pa_options_t(variant, math, num_stages, debug_flags, wait_limit_ns, ev)
+    opts = pa_options_t(variant, math, num_stages, debug_flags, wait_limit_ns, ev, ctas_per_sm, 0)
     _check(load_library().pa_forward(*_fwd_args(
         out, query, key_cache, value_cache, block_tables, seq_lens, scale, partition_size,
         workspace, max_seq_len, stream), ctypes.byref(opts)), "pa_forward")

@@ -93,6 +93,37 @@ pa_status_t ensure_smem(const void *fn, size_t bytes) {
   return PA_OK;
 }
 
+// Resident CTAs per SM of a kernel at a given block size and dynamic smem,
+// remembered per (kernel, smem, device).
+struct OccupancyEntry {
+  const void *fn;
+  int dev, threads;
+  size_t smem;
+  int per_sm;
+};
+OccupancyEntry g_occupancy[256];
+int g_num_occupancy = 0;
+
+pa_status_t occupancy(const void *fn, int threads, size_t smem, int *per_sm) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail_cuda("cudaGetDevice", e);
+  std::lock_guard<std::mutex> lock(g_mutex);
+  for (int i = 0; i < g_num_occupancy; ++i) {
+    const OccupancyEntry &o = g_occupancy[i];
+    if (o.fn == fn && o.dev == dev && o.threads == threads && o.smem == smem) {
+      *per_sm = o.per_sm;
+      return PA_OK;
+    }
+  }
+  int n = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, threads, smem);
+  if (e != cudaSuccess) return fail_cuda("cudaOccupancyMaxActiveBlocksPerMultiprocessor", e);
+  if (g_num_occupancy < 256) g_occupancy[g_num_occupancy++] = {fn, dev, threads, smem, n};
+  *per_sm = n;
+  return PA_OK;
+}
+
 // cuTensorMapEncodeTiled through the runtime's driver entry point (no
 // link-time dependency on libcuda).
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -269,6 +300,7 @@ pa_status_t launch(const Call &c, bool v2, const pa_options_t &opt) {
   p.block_tables = c.block_tables;
   p.seq_lens = c.seq_lens;
   p.status = reinterpret_cast<int *>(ws);
+  p.sched = reinterpret_cast<int *>(ws) + 1;
   if (v2) {
     p.max_logits = reinterpret_cast<float *>(ws + off[1]);
     p.exp_sums = reinterpret_cast<float *>(ws + off[2]);
@@ -296,12 +328,22 @@ pa_status_t launch(const Call &c, bool v2, const pa_options_t &opt) {
   st = ensure_smem(k.fn, smem);
   if (st != PA_OK) return st;
 
-  const long long grid = (long long)c.num_seqs * c.num_kv_heads * p.max_parts;
+  // Persistent grid: as many CTAs as fit on the GPU (or the requested number
+  // per SM), never more than there can be work items.
+  const int threads = (k.consumer_warps + 1) * 32;
+  int per_sm = 0;
+  st = occupancy(k.fn, threads, smem, &per_sm);
+  if (st != PA_OK) return st;
+  if (per_sm < 1) return PA_ERR_UNSUPPORTED;
+  if (opt.ctas_per_sm > 0 && opt.ctas_per_sm < per_sm) per_sm = opt.ctas_per_sm;
+  const long long max_items = (long long)c.num_seqs * c.num_kv_heads * p.max_parts;
+  long long grid = (long long)per_sm * dev->sm_count;
+  if (grid > max_items) grid = max_items;
   if (grid > 0) {
     cudaLaunchConfig_t cfg;
     memset(&cfg, 0, sizeof cfg);
     cfg.gridDim = dim3((unsigned)grid, 1, 1);
-    cfg.blockDim = dim3((unsigned)((k.consumer_warps + 1) * 32), 1, 1);
+    cfg.blockDim = dim3((unsigned)threads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = c.stream;
     void *args[3] = {&p, &tmap_k, &tmap_v};

@@ -1,19 +1,32 @@
-// Paged decode attention kernel: V1 (whole sequence per CTA) and Phase 1 of
-// V2 (one partition per CTA), per the "paged_attention_v2" commit note
-// (project_6, commit 96f4baf "Dockerfile", section "Implementation",
-// "Phase 1: Per-partition attention").
+// Paged decode attention kernel: V1 (whole sequence per work item) and
+// Phase 1 of V2 (one partition per work item), per the "paged_attention_v2"
+// commit note (project_6, commit 96f4baf "Dockerfile", section
+// "Implementation", "Phase 1: Per-partition attention").
 //
-// One CTA = one (sequence, KV head, token range).  It computes all G query
-// heads that share the KV head, so every K/V byte of the range crosses HBM
-// once.  Warp roles:
-//   warp NW        producer: reads the block table and issues TMA tile loads
-//                  of whole KV pages (128-byte swizzled panels) into a ring
-//                  of shared-memory stages, completing on mbarriers;
+// A work item is one (sequence, KV head, token range): the range is a
+// partition of partition_size tokens (V2) or the whole sequence (V1).  The
+// item computes all G query heads that share the KV head, so every K/V byte
+// of the range crosses HBM once.
+//
+// The kernel is persistent: a grid of about (CTAs per SM) x (SMs) CTAs pulls
+// items from a device-wide counter until none are left.  Warp roles in a CTA:
+//   warp NW        producer: takes the next item (atomic counter), locates it
+//                  (a warp scan over seq_lens for V2), reads its block-table
+//                  entries and issues TMA tile loads of whole KV pages
+//                  (128-byte swizzled panels) into a ring of shared-memory
+//                  stages, plus a bulk copy of the group's queries with the
+//                  item's first stage.  Each stage carries a small header
+//                  (item, first token, flags) written before its mbarrier
+//                  arrive.  The producer runs ahead into the next item while
+//                  the consumers finish the current one.
 //   warps 0..NW-1  consumers: each takes 16 tokens of every stage and keeps
 //                  its own online-softmax state (running max, sum, output).
-// At the end the consumer warps merge their states (the same log-sum-exp
-// combine as Phase 2) and write either the final output (V1) or the
-// partition's max_logits / exp_sums / normalised tmp_output (V2 Phase 1).
+//                  After an item's last stage they merge their states (the
+//                  same log-sum-exp combine as Phase 2) and write either the
+//                  final output (V1) or the partition's max_logits /
+//                  exp_sums / normalised tmp_output (V2 Phase 1).
+// The last CTA to finish resets the work counter, so the next launch on
+// the workspace starts from zero.
 //
 // Every wait is bounded (%globaltimer); a wait that runs out records
 // PA_ERR_DEVICE_TIMEOUT, the CTA lets its own in-flight copies land, and
@@ -31,6 +44,20 @@ namespace pa {
 constexpr int kStatusBadInput = 5;  // PA_ERR_DEVICE_BAD_INPUT
 constexpr int kStatusTimeout = 6;   // PA_ERR_DEVICE_TIMEOUT
 constexpr int kDebugStallConsumers = 1;
+
+constexpr int kStageFirst = 1;  // first stage of an item (carries the queries)
+constexpr int kStageLast = 2;   // last stage of an item (consumers write results)
+constexpr int kStageEnd = 4;    // no more items: consumers leave
+
+// Header of one ring stage, written by the producer before the stage's
+// mbarrier arrive and read by the consumers after their wait.
+struct StageInfo {
+  int s, kvh, part;  // the work item
+  int tok0;          // first token of the stage
+  int tok_end;       // end of the item's token range
+  int flags;         // kStage*
+  int pad[2];
+};
 
 // Geometry of one K (or V) stage buffer as TMA writes it:
 //   [unit][panel][unit_rows][128 bytes]
@@ -72,17 +99,17 @@ struct TensorMath {
   float m[NT][2];
   float l[NT][2];
 
-  __device__ __forceinline__ void init(const AttnParams &p, int s, int kvh, int lane, float *,
-                                       float *) {
-    const T *q = static_cast<const T *>(p.query) +
-                 ((size_t)s * p.num_heads + (size_t)kvh * p.group) * D;
+  // Start an item: queries of the group from shared memory ([G][D], input
+  // type), fresh softmax state.
+  __device__ __forceinline__ void begin_item(const uint8_t *q_smem, int group, int lane, int) {
+    const T *q = reinterpret_cast<const T *>(q_smem);
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       const int h = nt * 8 + (lane >> 2);
-      const bool live = h < p.group;
+      const bool live = h < group;
 #pragma unroll
       for (int ks = 0; ks < KS; ++ks) {
-        const T *src = q + (size_t)h * D + ks * 16 + 2 * (lane & 3);
+        const T *src = q + h * D + ks * 16 + 2 * (lane & 3);
         qf[nt][ks][0] = live ? *reinterpret_cast<const uint32_t *>(src) : 0u;
         qf[nt][ks][1] = live ? *reinterpret_cast<const uint32_t *>(src + 8) : 0u;
       }
@@ -95,15 +122,19 @@ struct TensorMath {
     }
   }
 
+  __device__ __forceinline__ void bind(float *, float *) {}
+
   __device__ __forceinline__ void tile(uint32_t kbase, uint32_t vbase, const StageGeom &g, int tok0,
                                        int valid, int lane, float scale_log2) {
     const int mi = lane >> 3, r = lane & 7;
     // ---- S^T = K Q^T
-    float sacc[NT][4];
+    // Two accumulators per n-tile (even / odd k-steps) halve the chain of
+    // dependent mma instructions.
+    float sacc[NT][4], sacc2[NT][4];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-      for (int j = 0; j < 4; ++j) sacc[nt][j] = 0.f;
+      for (int j = 0; j < 4; ++j) sacc[nt][j] = sacc2[nt][j] = 0.f;
     {
       const int tokA = tok0 + r + ((mi & 1) << 3);
       const uint32_t rowA = g.row_addr(kbase, tokA);
@@ -112,9 +143,17 @@ struct TensorMath {
         uint32_t a0, a1, a2, a3;
         ldsm_x4(g.chunk_addr(rowA, tokA, 2 * ks + (mi >> 1)), a0, a1, a2, a3);
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-          MmaOp<T>::run(sacc[nt], a0, a1, a2, a3, qf[nt][ks][0], qf[nt][ks][1]);
+        for (int nt = 0; nt < NT; ++nt) {
+          if (ks & 1)
+            MmaOp<T>::run(sacc2[nt], a0, a1, a2, a3, qf[nt][ks][0], qf[nt][ks][1]);
+          else
+            MmaOp<T>::run(sacc[nt], a0, a1, a2, a3, qf[nt][ks][0], qf[nt][ks][1]);
+        }
       }
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) sacc[nt][j] += sacc2[nt][j];
     }
     // ---- online softmax on the tile (log2 domain)
     const int t_lo = lane >> 2, t_hi = t_lo + 8;
@@ -178,10 +217,10 @@ struct TensorMath {
     }
   }
 
-  // Per-warp end state into shared memory: m_s/l_s [GMAX], o_s [GMAX][D+4].
-  __device__ __forceinline__ void store(float *m_s, float *l_s, float *o_s, int lane) {
+  // End of an item, step 1: this warp's max and sum per head -> m_w/l_w [GMAX].
+  __device__ __forceinline__ void stats(float *m_w, float *l_w, int lane) {
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
+    for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
         float v = l[nt][j];
@@ -190,18 +229,37 @@ struct TensorMath {
         v += __shfl_xor_sync(0xffffffffu, v, 16);
         if (lane < 4) {
           const int h = nt * 8 + 2 * lane + j;
-          m_s[h] = m[nt][j];
-          l_s[h] = v;
+          m_w[h] = m[nt][j];
+          l_w[h] = v;
         }
+      }
+  }
+
+  // Step 2: with every warp's stats in m_s/l_s [NW][GMAX], scale this warp's
+  // O by exp2(m_w - M) / L (log-sum-exp weight and final normaliser) and
+  // store it to o_w [GMAX][D+4]; the sum over warps is then the output.
+  __device__ __forceinline__ void store_scaled(float *o_w, const float *m_s, const float *l_s,
+                                               int nw, int lane) {
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      float f[2];
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int h = nt * 8 + 2 * (lane & 3) + j;
+        float M = -CUDART_INF_F;
+        for (int w = 0; w < nw; ++w) M = fmaxf(M, m_s[w * GMAX + h]);
+        float L = 0.f;
+        for (int w = 0; w < nw; ++w) L += l_s[w * GMAX + h] * exp2f(m_s[w * GMAX + h] - M);
+        f[j] = exp2f(m[nt][j] - M) / L;  // 0 for a warp that saw no token
       }
       const int h0 = nt * 8 + 2 * (lane & 3);
 #pragma unroll
       for (int mt = 0; mt < KS; ++mt) {
         const int d = mt * 16 + (lane >> 2);
-        o_s[h0 * (D + 4) + d] = o[nt][mt][0];
-        o_s[(h0 + 1) * (D + 4) + d] = o[nt][mt][1];
-        o_s[h0 * (D + 4) + d + 8] = o[nt][mt][2];
-        o_s[(h0 + 1) * (D + 4) + d + 8] = o[nt][mt][3];
+        o_w[h0 * (D + 4) + d] = o[nt][mt][0] * f[0];
+        o_w[(h0 + 1) * (D + 4) + d] = o[nt][mt][1] * f[1];
+        o_w[h0 * (D + 4) + d + 8] = o[nt][mt][2] * f[0];
+        o_w[(h0 + 1) * (D + 4) + d + 8] = o[nt][mt][3] * f[1];
       }
     }
   }
@@ -230,27 +288,27 @@ struct SimtMath {
     return g * QP + d + (d >= D / 2 ? 4 : 0);
   }
 
-  __device__ __forceinline__ void init(const AttnParams &, int, int, int, float *q_smem,
-                                       float *p_smem) {
+  __device__ __forceinline__ void bind(float *q_smem, float *p_smem) {
     q_s = q_smem;
     p_s = p_smem;
+  }
+
+  // Start an item: all consumer threads widen the group's queries ([G][D],
+  // input type, in shared memory) into the fp32 table q_s (the caller then
+  // synchronises the consumer warps).
+  __device__ __forceinline__ void begin_item(const uint8_t *q_smem, int group, int,
+                                             int ncons) {
+    const T *q = reinterpret_cast<const T *>(q_smem);
+    for (int i = threadIdx.x; i < GMAX * D; i += ncons) {
+      const int g = i / D, d = i % D;
+      const_cast<float *>(q_s)[qidx(g, d)] = g < group ? to_float(q[g * D + d]) : 0.f;
+    }
 #pragma unroll
     for (int g = 0; g < GMAX; ++g) {
       m[g] = -CUDART_INF_F;
       l[g] = 0.f;
 #pragma unroll
       for (int j = 0; j < DPL; ++j) acc[g][j] = 0.f;
-    }
-  }
-
-  // Cooperative load of the group's queries (all consumer threads).
-  __device__ static void load_q(const AttnParams &p, int s, int kvh, float *q_smem, int tid,
-                                int nthreads) {
-    const T *q = static_cast<const T *>(p.query) +
-                 ((size_t)s * p.num_heads + (size_t)kvh * p.group) * D;
-    for (int i = tid; i < GMAX * D; i += nthreads) {
-      const int g = i / D, d = i % D;
-      q_smem[qidx(g, d)] = g < p.group ? to_float(q[(size_t)g * D + d]) : 0.f;
     }
   }
 
@@ -370,25 +428,46 @@ struct SimtMath {
     __syncwarp();
   }
 
-  __device__ __forceinline__ void store(float *m_s, float *l_s, float *o_s, int lane) {
+  __device__ __forceinline__ void stats(float *m_w, float *l_w, int lane) {
 #pragma unroll
     for (int gg = 0; gg < GMAX; ++gg) {
       float v = l[gg];
 #pragma unroll
       for (int off = 1; off < 16; off <<= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
       if (lane == 0) {
-        m_s[gg] = m[gg];
-        l_s[gg] = v;
+        m_w[gg] = m[gg];
+        l_w[gg] = v;
       }
+    }
+  }
+
+  __device__ __forceinline__ void store_scaled(float *o_w, const float *m_s, const float *l_s,
+                                               int nw, int lane) {
 #pragma unroll
-      for (int j = 0; j < DPL; ++j) o_s[gg * (D + 4) + lane * DPL + j] = acc[gg][j];
+    for (int gg = 0; gg < GMAX; ++gg) {
+      float M = -CUDART_INF_F;
+      for (int w = 0; w < nw; ++w) M = fmaxf(M, m_s[w * GMAX + gg]);
+      float L = 0.f;
+      for (int w = 0; w < nw; ++w) L += l_s[w * GMAX + gg] * exp2f(m_s[w * GMAX + gg] - M);
+      const float f = exp2f(m[gg] - M) / L;
+#pragma unroll
+      for (int j = 0; j < DPL; ++j) o_w[gg * (D + 4) + lane * DPL + j] = acc[gg][j] * f;
     }
   }
 };
 
+// Register cap per thread: three CTAs of (NW + 1) warps must fit in one SM,
+// i.e. at most four warps' registers per SM sub-partition (16K registers).
+// (Groups of more than 8 heads keep twice the accumulators; they are left
+// uncapped rather than spill.)
+template <int NW, int GMAX>
+constexpr int kernel_max_regs() {
+  return GMAX > 8 ? 255 : (NW == 4 ? 128 : (NW == 2 ? 168 : 255));
+}
+
 // ---------------------------------------------------------------------------
 template <typename T, int D, int NW, int GMAX, class Math, bool SIMT>
-__global__ void __launch_bounds__((NW + 1) * 32, 1)
+__global__ void __launch_bounds__((NW + 1) * 32, 1) __maxnreg__((kernel_max_regs<NW, GMAX>()))
     pa_attn_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CUtensorMap tmap_k,
                    const __grid_constant__ CUtensorMap tmap_v) {
   constexpr int ELT = sizeof(T);
@@ -397,44 +476,34 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1)
   constexpr int NPANELS = ROW_BYTES / kPanelBytes;
   constexpr int HALF_BYTES = ST * ROW_BYTES;  // K (or V) bytes of one stage
   constexpr int NCONS = NW * 32;
+  constexpr int QBYTES = GMAX * D * ELT;      // query slot of one stage
+  // The consumer warps merge their states in the K/V bytes of an item's last
+  // stage when they fit (the data is dead by then; the slot is released after
+  // the merge), else in a dedicated area.
+  constexpr int MERGE_BYTES = NW * GMAX * (D + 4) * 4 + NW * GMAX * 2 * 4;
+  constexpr bool MERGE_IN_SLOT = MERGE_BYTES <= 2 * HALF_BYTES;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int part = blockIdx.x % p.max_parts;
-  const int sk = blockIdx.x / p.max_parts;
-  const int kvh = sk % p.num_kv_heads;
-  const int s = sk / p.num_kv_heads;
-
-  int L = p.seq_lens[s];
-  if (L < 0 || L > p.max_seq_len) {
-    if (threadIdx.x == 0 && part == 0 && kvh == 0) report(p.status, kStatusBadInput);
-    L = L < 0 ? 0 : p.max_seq_len;
-  }
-  const int tok_begin = part * p.range_tokens;
-  if (tok_begin >= L) {
-    if (!p.write_partials && part == 0) {  // V1, empty sequence: zeros
-      T *o = static_cast<T *>(p.out) + ((size_t)s * p.num_heads + (size_t)kvh * p.group) * D;
-      for (int i = threadIdx.x; i < p.group * D; i += blockDim.x) o[i] = from_float<T>(0.f);
-    }
-    return;
-  }
-  const int tok_end = min(tok_begin + p.range_tokens, L);
-  const int n_stages = (tok_end - tok_begin + ST - 1) / ST;
   const int NST = p.num_stages;
 
-  // ---- shared memory carve-up
+  // ---- shared memory carve-up (sizes mirrored by attn_smem_bytes)
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const size_t ring_bytes = (size_t)NST * 2 * HALF_BYTES;
-  const size_t merge_bytes = (size_t)NW * GMAX * (D + 4) * 4 + (size_t)NW * GMAX * 2 * 4;
-  const size_t body = ring_bytes > merge_bytes ? ring_bytes : merge_bytes;
-  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + body);
-  volatile int *flags = reinterpret_cast<volatile int *>(bars + 2 * NST + 1);
+  uint8_t *ring = smem;
+  uint8_t *qbuf = ring + (size_t)NST * 2 * HALF_BYTES;
+  uint8_t *merge_area = qbuf + (size_t)NST * QBYTES;
+  StageInfo *info =
+      reinterpret_cast<StageInfo *>(merge_area + (MERGE_IN_SLOT ? 0 : MERGE_BYTES));
+  uint64_t *bars = reinterpret_cast<uint64_t *>(info + NST);
+  volatile int *flags = reinterpret_cast<volatile int *>(bars + 2 * NST + 2);
   float *simt_q = reinterpret_cast<float *>(
-      (reinterpret_cast<uintptr_t>(flags) + 16 + 15) & ~uintptr_t(15));  // 16-byte aligned
+      (reinterpret_cast<uintptr_t>(flags) + 16 + 15) & ~uintptr_t(15));
   float *simt_p = simt_q + GMAX * (D + 8);
-  const uint32_t ring_u32 = smem_u32(smem);
+  const uint32_t ring_u32 = smem_u32(ring);
+  const uint32_t qbuf_u32 = smem_u32(qbuf);
   const uint32_t full0 = smem_u32(bars), empty0 = full0 + 8 * NST, never = full0 + 16 * NST;
+  const uint32_t cons_bar = never + 8;  // consumer-warp barrier (bounded waits)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < NST; ++i) {
@@ -442,17 +511,16 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1)
       mbar_init(empty0 + 8 * i, NW);
     }
     mbar_init(never, 1);
+    mbar_init(cons_bar, NW);
     flags[0] = 0;
     fence_mbar_init();
-  }
-  if constexpr (SIMT) {
-    if (warp < NW) Math::load_q(p, s, kvh, simt_q, threadIdx.x, NCONS);
   }
   __syncthreads();
 
   const StageGeom geom{p.log2_unit_rows, p.unit_rows - 1, (uint32_t)p.unit_rows * kPanelBytes,
                        (uint32_t)(NPANELS * p.unit_rows * kPanelBytes)};
   const uint64_t limit = p.wait_limit_ns;
+  const int qbytes = p.group * D * ELT;
 
   if (warp == NW) {
     // ======================= producer warp =======================
@@ -460,141 +528,302 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1)
       prefetch_tmap(&tmap_k);
       prefetch_tmap(&tmap_v);
     }
-    const int32_t *bt = p.block_tables + (size_t)s * p.max_blocks_per_seq;
     const int U = p.unit_rows;
     const int units_per_stage = ST / U;
-    const int last_page = (tok_end - 1) >> p.log2_block_size;
-    // A window of 64 block-table entries: lane i holds pages win0+i (cur)
-    // and win0+32+i (nxt); it slides by 32 pages when a stage reaches nxt.
-    int win0 = tok_begin >> p.log2_block_size;
-    auto load_entry = [&](int page) -> int { return page <= last_page ? __ldg(bt + page) : -1; };
-    int cur = load_entry(win0 + lane);
-    int nxt = load_entry(win0 + 32 + lane);
-    int issued = 0;
+    // The first item of a CTA is its own index; later ones come from the
+    // counter, offset by the grid.  Lane 0 issues the atomic one item ahead
+    // and the value is broadcast only when that item is located.
+    auto grab_issue = [&]() -> int { return lane == 0 ? atomicAdd(p.sched, 1) : 0; };
+    auto grab_value = [&](int raw) -> int {
+      return (int)gridDim.x + __shfl_sync(0xffffffffu, raw, 0);
+    };
+    // V2 locates an item through the running count of items per sequence;
+    // the cursor (a chunk of 32 sequences, scanned once) only moves forward
+    // because every CTA takes items in increasing order.
+    int cs = 0, cbase = 0, c_cnt = 0, c_incl = 0, c_L = 0, c_total = 0;
+    bool c_loaded = false;
+    int i = 0;  // stages issued by this CTA
     bool ok = true;
-    for (int i = 0; i < n_stages; ++i) {
+    int item = blockIdx.x;
+    while (true) {
+      // ---- locate the item: (s, kvh, part, L)
+      int s = 0, kvh = 0, part = 0, L = 0;
+      bool found = false;
+      if (!p.write_partials) {  // V1: Hkv items per sequence, empty ones too
+        s = item / p.num_kv_heads;
+        if (s < p.num_seqs) {
+          found = true;
+          kvh = item % p.num_kv_heads;
+          L = __ldg(p.seq_lens + s);
+          if (L < 0 || L > p.max_seq_len) {
+            if (lane == 0) report(p.status, kStatusBadInput);
+            L = L < 0 ? 0 : p.max_seq_len;
+          }
+        }
+      } else {
+        while (true) {
+          if (!c_loaded) {
+            const int sl = cs + lane;
+            c_L = 0;
+            if (sl < p.num_seqs) {
+              c_L = __ldg(p.seq_lens + sl);
+              if (c_L < 0 || c_L > p.max_seq_len) {
+                report(p.status, kStatusBadInput);
+                c_L = c_L < 0 ? 0 : p.max_seq_len;
+              }
+            }
+            c_cnt = p.num_kv_heads * ((c_L + p.range_tokens - 1) / p.range_tokens);
+            c_incl = c_cnt;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+              const int t = __shfl_up_sync(0xffffffffu, c_incl, off);
+              if (lane >= off) c_incl += t;
+            }
+            c_total = __shfl_sync(0xffffffffu, c_incl, 31);
+            c_loaded = true;
+          }
+          if (item < cbase + c_total) {
+            const unsigned hit = __ballot_sync(0xffffffffu, cbase + c_incl > item);
+            const int ls = __ffs(hit) - 1;
+            s = cs + ls;
+            L = __shfl_sync(0xffffffffu, c_L, ls);
+            const int first = cbase + __shfl_sync(0xffffffffu, c_incl - c_cnt, ls);
+            const int np = (L + p.range_tokens - 1) / p.range_tokens;
+            kvh = (item - first) / np;
+            part = (item - first) % np;
+            found = true;
+            break;
+          }
+          if (cs + 32 >= p.num_seqs) break;
+          cs += 32;
+          cbase += c_total;
+          c_loaded = false;
+        }
+      }
+      if (!found) break;
+      const int next_raw = grab_issue();  // its latency overlaps this item's stages
+
+      const int tok_begin = part * p.range_tokens;
+      const int tok_end = min(tok_begin + p.range_tokens, L);
+      if (tok_end <= tok_begin) {  // V1, empty sequence: zeros
+        T *o = static_cast<T *>(p.out) + ((size_t)s * p.num_heads + (size_t)kvh * p.group) * D;
+        for (int e = lane; e < p.group * D; e += 32) o[e] = from_float<T>(0.f);
+        item = grab_value(next_raw);
+        continue;
+      }
+      // A window of 64 block-table entries: lane j holds pages win0+j (cur)
+      // and win0+32+j (nxt); it slides by 32 pages when a stage reaches nxt.
+      const int32_t *bt = p.block_tables + (size_t)s * p.max_blocks_per_seq;
+      const int last_page = (tok_end - 1) >> p.log2_block_size;
+      auto load_entry = [&](int page) -> int { return page <= last_page ? __ldg(bt + page) : -1; };
+      int win0 = tok_begin >> p.log2_block_size;
+      int cur = load_entry(win0 + lane);
+      int nxt = load_entry(win0 + 32 + lane);
+      const int n_st = (tok_end - tok_begin + ST - 1) / ST;
+      for (int j = 0; j < n_st; ++j) {
+        const int st = i % NST;
+        if (i >= NST) {
+          bool w = true;
+          if (lane == 0) w = mbar_wait(empty0 + 8 * st, ((i / NST) - 1) & 1, limit, flags);
+          ok = __shfl_sync(0xffffffffu, w, 0);
+          if (!ok) break;
+        }
+        const int stage_tok0 = tok_begin + j * ST;
+        const int n_units = min(units_per_stage, (tok_end - stage_tok0 + U - 1) / U);
+        const int tok = stage_tok0 + lane * U;
+        const int rel = ((lane < n_units ? tok : stage_tok0) >> p.log2_block_size) - win0;
+        const int a = __shfl_sync(0xffffffffu, cur, rel & 31);
+        const int b = __shfl_sync(0xffffffffu, nxt, rel & 31);
+        int y = -1;
+        if (lane < n_units) {
+          const int blk = rel < 32 ? a : b;
+          if ((unsigned)blk >= (unsigned)p.num_blocks) {
+            report(p.status, kStatusBadInput);
+          } else {
+            y = (blk * p.num_kv_heads + kvh) * p.block_size + (tok & (p.block_size - 1));
+          }
+        }
+        const unsigned valid_mask = __ballot_sync(0xffffffffu, y >= 0);
+        const bool first = j == 0;
+        if (lane == 0) {
+          StageInfo &h = info[st];
+          h.s = s;
+          h.kvh = kvh;
+          h.part = part;
+          h.tok0 = stage_tok0;
+          h.tok_end = tok_end;
+          h.flags = (first ? kStageFirst : 0) | (j == n_st - 1 ? kStageLast : 0);
+          mbar_arrive_expect_tx(full0 + 8 * st, (uint32_t)__popc(valid_mask) * U * ROW_BYTES * 2 +
+                                                    (first ? (uint32_t)qbytes : 0u));
+        }
+        __syncwarp();
+        if (y >= 0) {
+          const uint32_t kdst = ring_u32 + (uint32_t)st * 2 * HALF_BYTES + (uint32_t)lane * geom.unit_bytes;
+          const uint32_t vdst = kdst + HALF_BYTES;
+#pragma unroll
+          for (int pn = 0; pn < NPANELS; ++pn) {
+            tma_load_2d(kdst + pn * geom.panel_bytes, &tmap_k, pn * (kPanelBytes / ELT), y, full0 + 8 * st);
+            tma_load_2d(vdst + pn * geom.panel_bytes, &tmap_v, pn * (kPanelBytes / ELT), y, full0 + 8 * st);
+          }
+        }
+        if (first && lane == 0) {
+          const T *q = static_cast<const T *>(p.query) +
+                       ((size_t)s * p.num_heads + (size_t)kvh * p.group) * D;
+          bulk_load(qbuf_u32 + (uint32_t)st * QBYTES, q, (uint32_t)qbytes, full0 + 8 * st);
+        }
+        ++i;
+        const int next_rel = ((stage_tok0 + ST) >> p.log2_block_size) - win0;
+        if (next_rel >= 32) {
+          cur = nxt;
+          win0 += 32;
+          nxt = load_entry(win0 + 32 + lane);
+        }
+      }
+      if (!ok) break;
+      item = grab_value(next_raw);
+    }
+    if (ok) {  // tell the consumers there is nothing more
       const int st = i % NST;
       if (i >= NST) {
         bool w = true;
         if (lane == 0) w = mbar_wait(empty0 + 8 * st, ((i / NST) - 1) & 1, limit, flags);
         ok = __shfl_sync(0xffffffffu, w, 0);
-        if (!ok) break;
       }
-      const int stage_tok0 = tok_begin + i * ST;
-      const int n_units = min(units_per_stage, (tok_end - stage_tok0 + U - 1) / U);
-      const int tok = stage_tok0 + lane * U;
-      const int rel = ((lane < n_units ? tok : stage_tok0) >> p.log2_block_size) - win0;
-      const int a = __shfl_sync(0xffffffffu, cur, rel & 31);
-      const int b = __shfl_sync(0xffffffffu, nxt, rel & 31);
-      int y = -1;
-      if (lane < n_units) {
-        const int blk = rel < 32 ? a : b;
-        if ((unsigned)blk >= (unsigned)p.num_blocks) {
-          report(p.status, kStatusBadInput);
-        } else {
-          y = (blk * p.num_kv_heads + kvh) * p.block_size + (tok & (p.block_size - 1));
-        }
+      if (ok && lane == 0) {
+        info[st].flags = kStageEnd;
+        mbar_arrive(full0 + 8 * st);
       }
-      const unsigned valid_mask = __ballot_sync(0xffffffffu, y >= 0);
-      if (lane == 0)
-        mbar_arrive_expect_tx(full0 + 8 * st, (uint32_t)__popc(valid_mask) * U * ROW_BYTES * 2);
-      __syncwarp();
-      if (y >= 0) {
-        const uint32_t kdst = ring_u32 + (uint32_t)st * 2 * HALF_BYTES + (uint32_t)lane * geom.unit_bytes;
-        const uint32_t vdst = kdst + HALF_BYTES;
-#pragma unroll
-        for (int pn = 0; pn < NPANELS; ++pn) {
-          tma_load_2d(kdst + pn * geom.panel_bytes, &tmap_k, pn * (kPanelBytes / ELT), y, full0 + 8 * st);
-          tma_load_2d(vdst + pn * geom.panel_bytes, &tmap_v, pn * (kPanelBytes / ELT), y, full0 + 8 * st);
-        }
-      }
-      ++issued;
-      // slide the window once the next stage starts in the nxt half
-      const int next_rel = ((stage_tok0 + ST) >> p.log2_block_size) - win0;
-      if (next_rel >= 32) {
-        cur = nxt;
-        win0 += 32;
-        nxt = load_entry(win0 + 32 + lane);
-      }
+      if (ok) ++i;
     }
-    if (!ok) {
+    if (!ok && lane == 0) {
       report(p.status, kStatusTimeout);
       flags[0] = 1;
     }
     // Let every copy this CTA started land before the CTA can retire.
     if (lane == 0) {
-      const int first = issued > NST ? issued - NST : 0;
-      for (int j = first; j < issued; ++j)
+      const int first = i > NST ? i - NST : 0;
+      for (int j = first; j < i; ++j)
         mbar_wait(full0 + 8 * (j % NST), (j / NST) & 1, kDrainLimitNs, nullptr);
     }
     __syncwarp();
-    return;
-  }
-
-  // ======================= consumer warps =======================
-  Math math;
-  math.init(p, s, kvh, lane, simt_q, simt_p + warp * kTileTokens * GMAX);
-  bool ok = true;
-  if (p.debug_flags & kDebugStallConsumers) {
-    // Wait on a barrier that nothing releases: the bound must end it.
-    ok = mbar_wait(never, 0, limit, flags);
-    ok = __all_sync(0xffffffffu, ok);
-  }
-  for (int i = 0; ok && i < n_stages; ++i) {
-    const int st = i % NST;
-    bool w = mbar_wait(full0 + 8 * st, (i / NST) & 1, limit, flags);
-    ok = __all_sync(0xffffffffu, w);
-    if (!ok) break;
-    const int tile_tok0 = tok_begin + i * ST + warp * kTileTokens;
-    const int valid = max(0, min(kTileTokens, tok_end - tile_tok0));
-    if (valid > 0) {
-      const uint32_t kbase = ring_u32 + (uint32_t)st * 2 * HALF_BYTES;
-      math.tile(kbase, kbase + HALF_BYTES, geom, warp * kTileTokens, valid, lane, p.scale_log2);
+  } else {
+    // ======================= consumer warps =======================
+    Math math;
+    math.bind(simt_q, simt_p + warp * kTileTokens * GMAX);
+    // Barrier of the NW consumer warps on an mbarrier, so that its wait is
+    // bounded like every other wait (a plain bar.sync could not give up).
+    int cons_phase = 0;
+    auto cons_sync = [&]() -> bool {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(cons_bar);
+      const bool w = mbar_wait(cons_bar, cons_phase & 1, limit, flags);
+      ++cons_phase;
+      return __all_sync(0xffffffffu, w);
+    };
+    bool ok = true;
+    if (p.debug_flags & kDebugStallConsumers) {
+      // Wait on a barrier that nothing releases: the bound must end it.
+      ok = mbar_wait(never, 0, limit, flags);
+      ok = __all_sync(0xffffffffu, ok);
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(empty0 + 8 * st);
-  }
-  if (!ok) {
-    if (lane == 0) {
+    for (int i = 0; ok; ++i) {
+      const int st = i % NST;
+      const bool w = mbar_wait(full0 + 8 * st, (i / NST) & 1, limit, flags);
+      ok = __all_sync(0xffffffffu, w);
+      if (!ok) break;
+      const StageInfo h = info[st];
+      if (h.flags & kStageEnd) break;
+      if (h.flags & kStageFirst) {
+        math.begin_item(qbuf + (size_t)st * QBYTES, p.group, lane, NCONS);
+        if constexpr (SIMT) {
+          ok = cons_sync();  // the shared fp32 query table is complete
+          if (!ok) break;
+        }
+      }
+      const int tile_tok0 = h.tok0 + warp * kTileTokens;
+      const int valid = max(0, min(kTileTokens, h.tok_end - tile_tok0));
+      if (valid > 0) {
+        const uint32_t kbase = ring_u32 + (uint32_t)st * 2 * HALF_BYTES;
+        math.tile(kbase, kbase + HALF_BYTES, geom, warp * kTileTokens, valid, lane, p.scale_log2);
+      }
+      __syncwarp();
+      if (!(h.flags & kStageLast)) {
+        if (lane == 0) mbar_arrive(empty0 + 8 * st);
+        continue;
+      }
+
+      // ---- item done: merge the consumer warps' states (log-sum-exp), write
+      uint8_t *mb = MERGE_IN_SLOT ? ring + (size_t)st * 2 * HALF_BYTES : merge_area;
+      float *m_s = reinterpret_cast<float *>(mb);
+      float *l_s = m_s + NW * GMAX;
+      float *o_s = l_s + NW * GMAX;
+      ok = cons_sync();  // every warp is done with the slot's K/V (and the previous merge)
+      if (!ok) break;
+      math.stats(m_s + warp * GMAX, l_s + warp * GMAX, lane);
+      ok = cons_sync();
+      if (!ok) break;
+      math.store_scaled(o_s + (size_t)warp * GMAX * (D + 4), m_s, l_s, NW, lane);
+      ok = cons_sync();
+      if (!ok) break;
+      // out[h][d] = sum over warps of the scaled partial outputs (16 bytes a thread)
+      const int G = p.group;
+      const size_t head0 = (size_t)h.s * p.num_heads + (size_t)h.kvh * G;
+      for (int idx = threadIdx.x; idx < G * (D / 4); idx += NCONS) {
+        const int hh = idx / (D / 4), d = 4 * (idx % (D / 4));
+        float4 acc = *reinterpret_cast<const float4 *>(&o_s[(size_t)hh * (D + 4) + d]);
+#pragma unroll
+        for (int w2 = 1; w2 < NW; ++w2) {
+          const float4 v =
+              *reinterpret_cast<const float4 *>(&o_s[((size_t)w2 * GMAX + hh) * (D + 4) + d]);
+          acc.x += v.x;
+          acc.y += v.y;
+          acc.z += v.z;
+          acc.w += v.w;
+        }
+        if (p.write_partials) {
+          const size_t row = (head0 + hh) * p.max_parts + h.part;
+          *reinterpret_cast<float4 *>(p.tmp_out + row * D + d) = acc;
+          if (d == 0) {
+            float M = -CUDART_INF_F;
+#pragma unroll
+            for (int w2 = 0; w2 < NW; ++w2) M = fmaxf(M, m_s[w2 * GMAX + hh]);
+            float L = 0.f;
+#pragma unroll
+            for (int w2 = 0; w2 < NW; ++w2) L += l_s[w2 * GMAX + hh] * exp2f(m_s[w2 * GMAX + hh] - M);
+            p.max_logits[row] = M * 0.69314718055994530942f;  // back to natural-log units
+            p.exp_sums[row] = L;
+          }
+        } else {
+          T *o = static_cast<T *>(p.out) + (head0 + hh) * D + d;
+          o[0] = from_float<T>(acc.x);
+          o[1] = from_float<T>(acc.y);
+          o[2] = from_float<T>(acc.z);
+          o[3] = from_float<T>(acc.w);
+        }
+      }
+      if (MERGE_IN_SLOT) {
+        // hand the slot back to the producer; its next TMA writes come after
+        // our generic-proxy writes
+        fence_proxy_async_smem();
+        ok = cons_sync();
+        if (!ok) break;
+      }
+      if (lane == 0) mbar_arrive(empty0 + 8 * st);
+    }
+    if (!ok && lane == 0) {
       report(p.status, kStatusTimeout);
       flags[0] = 1;
     }
+    pdl_launch_dependents();
   }
-  named_bar_sync(1, NCONS);
-  if (flags[0]) return;
-  pdl_launch_dependents();
 
-  // ---- merge the consumer warps' states (log-sum-exp) and write out
-  float *m_s = reinterpret_cast<float *>(smem);
-  float *l_s = m_s + NW * GMAX;
-  float *o_s = l_s + NW * GMAX;
-  math.store(m_s + warp * GMAX, l_s + warp * GMAX, o_s + (size_t)warp * GMAX * (D + 4), lane);
-  named_bar_sync(1, NCONS);
-
-  const int G = p.group;
-  const size_t head0 = (size_t)s * p.num_heads + (size_t)kvh * G;
-  for (int idx = threadIdx.x; idx < G * D; idx += NCONS) {
-    const int h = idx / D, d = idx % D;
-    float M = -CUDART_INF_F;
-#pragma unroll
-    for (int w = 0; w < NW; ++w) M = fmaxf(M, m_s[w * GMAX + h]);
-    float acc = 0.f, lsum = 0.f;
-#pragma unroll
-    for (int w = 0; w < NW; ++w) {
-      const float f = exp2f(m_s[w * GMAX + h] - M);  // 0 for warps that saw no token
-      acc += f * o_s[((size_t)w * GMAX + h) * (D + 4) + d];
-      lsum += f * l_s[w * GMAX + h];
-    }
-    const float val = acc / lsum;
-    if (p.write_partials) {
-      const size_t row = (head0 + h) * p.max_parts + part;
-      p.tmp_out[row * D + d] = val;
-      if (d == 0) {
-        p.max_logits[row] = M * 0.69314718055994530942f;  // back to natural-log units
-        p.exp_sums[row] = lsum;
-      }
-    } else {
-      static_cast<T *>(p.out)[(head0 + h) * D + d] = from_float<T>(val);
+  // ---- the last CTA out resets the work counter for the next launch
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(p.sched + 1, 1) == (int)gridDim.x - 1) {
+      atomicExch(p.sched, 0);
+      atomicExch(p.sched + 1, 0);
     }
   }
 }

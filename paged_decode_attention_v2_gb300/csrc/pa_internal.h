@@ -23,12 +23,13 @@ struct AttnParams {
   float *exp_sums;             // [B][H][max_parts]   (V2)
   float *tmp_out;              // [B][H][max_parts][D] (V2)
   int *status;                 // workspace status word
+  int *sched;                  // [0] next work item, [1] CTAs finished (reset by the last)
   int num_seqs, num_heads, num_kv_heads, group;  // group = H / Hkv
   int block_size, log2_block_size;
   int unit_rows, log2_unit_rows;  // rows per TMA box: min(block_size, stage tokens)
   int max_blocks_per_seq, max_seq_len, num_blocks;
-  int range_tokens;   // tokens per CTA: partition_size (V2) or whole sequence (V1)
-  int max_parts;      // CTAs per (seq, kv head)
+  int range_tokens;   // tokens per work item: partition_size (V2) or max_seq_len (V1)
+  int max_parts;      // partitions per (seq, head) in the workspace layout
   int write_partials; // 1: V2 Phase 1 outputs, 0: V1 final output
   int num_stages;
   int debug_flags;
@@ -57,21 +58,26 @@ struct AttnKernelInfo {
   int max_group;      // largest H / Hkv it handles
 };
 
-// Dynamic shared memory the attention kernel needs for `stages` stages.
+// Dynamic shared memory the attention kernel needs for `stages` stages (the
+// kernel's carve-up, in order: ring, query slots, merge area, stage headers,
+// mbarriers, flags, CUDA-core tables).
 inline size_t attn_smem_bytes(int head_size, int elt, int consumer_warps, int max_group,
                               int stages, bool simt) {
   size_t stage = (size_t)consumer_warps * kTileTokens * head_size * elt * 2;
   size_t ring = stage * stages;
+  size_t qslots = (size_t)max_group * head_size * elt * stages;
   size_t merge = (size_t)consumer_warps * max_group * (head_size + 4) * 4 +
                  (size_t)consumer_warps * max_group * 2 * 4;
-  size_t body = ring > merge ? ring : merge;
-  size_t bars = 2 * 8 * (size_t)stages + 8 + 16 + 16;  // full/empty/never-set, flags, pad
+  if (merge <= stage) merge = 0;  // merged inside the item's last stage
+  size_t headers = 32 * (size_t)stages;
+  size_t bars = 8 * (2 * (size_t)stages + 2);  // full, empty, never-set, consumer barrier
+  size_t flags = 16 + 16;                      // flags + alignment
   size_t simt_extra = 0;
   if (simt) {
-    simt_extra = (size_t)max_group * (head_size + 8) * 4 +                    // q (fp32)
-                 (size_t)consumer_warps * kTileTokens * max_group * 4;       // p tiles
+    simt_extra = (size_t)max_group * (head_size + 8) * 4 +               // q (fp32)
+                 (size_t)consumer_warps * kTileTokens * max_group * 4;  // p tiles
   }
-  return 1024 /* alignment slack */ + body + bars + simt_extra + 64;
+  return 1024 /* alignment slack */ + ring + qslots + merge + headers + bars + flags + simt_extra;
 }
 
 // Kernel tables, one per translation unit (see pa_attn_*.cu).
