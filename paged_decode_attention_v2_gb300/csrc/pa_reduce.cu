@@ -7,14 +7,13 @@
 //
 // A group of `wph` warps (1, 2, 4 or 8) serves one (sequence, query head) and
 // a slice of `cols_per_cta` columns of it; a 256-thread CTA holds 8 / wph such
-// groups.  Every warp of a group finds M and sum r_p over all partitions by
-// itself (warp shuffles, no block barrier), then takes every wph-th
-// partition and accumulates r_p * tmp_out[p] over its columns with 16-byte
-// loads, four partitions in flight.  With wph > 1 the warps' partial sums
-// meet once in shared memory.  One warp per head suits batches whose
-// sequences span few partitions; long sequences split their partitions over
-// up to 8 warps (and their columns over several CTAs) to keep the load chain
-// short.
+// groups.  Lanes form row groups of `lpr` lanes (one 16-byte column chunk
+// each); every row group walks its share of the partitions in one pass,
+// four at a time with all loads issued up front, keeping an online
+// log-sum-exp state: running max m, running sum S = sum r_p exp(-m) and the
+// running weighted row sum.  Row groups, then warps (through shared memory),
+// merge their states with the same rescale rule, so the result is the
+// formula above up to rounding.
 #include <math_constants.h>
 
 #include "pa_device.cuh"
@@ -23,6 +22,29 @@ namespace pa {
 
 constexpr int kReduceThreads = 256;
 
+// Online LSE state of one lane: max, normaliser and up to 8 columns.
+struct LseAcc {
+  float m, S;
+  float4 a[2];
+};
+
+__device__ __forceinline__ void lse_merge(LseAcc &x, float m2, float S2, const float4 (&a2)[2],
+                                          int per_lane) {
+  const float M = fmaxf(x.m, m2);
+  const float f1 = M == -CUDART_INF_F ? 0.f : expf(x.m - M);
+  const float f2 = M == -CUDART_INF_F ? 0.f : expf(m2 - M);
+  x.S = x.S * f1 + S2 * f2;
+#pragma unroll
+  for (int k = 0; k < 2; ++k)
+    if (k < per_lane) {
+      x.a[k].x = x.a[k].x * f1 + a2[k].x * f2;
+      x.a[k].y = x.a[k].y * f1 + a2[k].y * f2;
+      x.a[k].z = x.a[k].z * f1 + a2[k].z * f2;
+      x.a[k].w = x.a[k].w * f1 + a2[k].w * f2;
+    }
+  x.m = M;
+}
+
 template <typename OutT>
 __global__ void __launch_bounds__(kReduceThreads)
     pa_v2_reduce_kernel(const __grid_constant__ ReduceParams p) {
@@ -30,7 +52,8 @@ __global__ void __launch_bounds__(kReduceThreads)
   // has finished; wait here until all of its results are visible.
   pdl_wait_primary();
 
-  __shared__ float4 part_sum[kReduceThreads / 32][64];  // [warp][<= 256 cols / 4]
+  __shared__ float4 part_a[kReduceThreads / 32][64];  // [warp][<= 256 cols / 4]
+  __shared__ float part_m[kReduceThreads / 32], part_S[kReduceThreads / 32];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int wph = p.warps_per_head;
   const int groups = (kReduceThreads / 32) / wph;
@@ -49,108 +72,111 @@ __global__ void __launch_bounds__(kReduceThreads)
     L = L < 0 ? 0 : (L > p.max_seq_len ? p.max_seq_len : L);  // Phase 1 reported it
     np = (L + p.partition_size - 1) / p.partition_size;
   }
-  OutT *out = static_cast<OutT *>(p.out) + ((size_t)s * p.num_heads + h) * D + col0;
   const size_t row0 = ((size_t)s * p.num_heads + h) * p.max_parts;
   const float *ml = p.max_logits + row0;
   const float *es = p.exp_sums + row0;
 
-  // ---- M and the normaliser, per warp
-  float mx = -CUDART_INF_F;
-  for (int i = lane; i < np; i += 32) mx = fmaxf(mx, __ldcg(ml + i));
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-  float wsum = 0.f;
-  for (int i = lane; i < np; i += 32) wsum += expf(__ldcg(ml + i) - mx) * __ldcg(es + i);
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, off);
-
-  // ---- weighted sum over this warp's partitions
-  // lanes: `lpr` lanes per row (one float4 each, several if ncols > 128),
-  // `rpi` rows per warp iteration
-  const int c4 = ncols / 4;                // float4s per row
-  const int lpr = c4 < 32 ? c4 : 32;       // lanes per row
-  const int rpi = 32 / lpr;                // rows per iteration
-  const int per_lane = c4 / lpr;           // float4s per lane (1 or 2)
+  const int c4 = ncols / 4;           // float4s per row
+  const int lpr = c4 < 32 ? c4 : 32;  // lanes per row
+  const int rpi = 32 / lpr;           // rows per warp iteration
+  const int per_lane = c4 / lpr;      // float4s per lane (1 or 2)
   const int sub = lane / lpr, cl = lane % lpr;
-  float4 acc[2] = {make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
   const float *tmp = p.tmp_out + row0 * D + col0 + 4 * cl;
   const int stride = wph * rpi;
+
+  LseAcc acc;
+  acc.m = -CUDART_INF_F;
+  acc.S = 0.f;
+  acc.a[0] = acc.a[1] = make_float4(0.f, 0.f, 0.f, 0.f);
   int i = wig * rpi + sub;
-  for (; i + 3 * stride < np; i += 4 * stride) {
+  for (; i < np; i += 4 * stride) {
+    float lm[4], le[4];
     float4 v[4][2];
-    float w[4];
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int r = i + u * stride;
-      w[u] = expf(__ldcg(ml + r) - mx) * __ldcg(es + r);
+      const bool ok = r < np;
+      lm[u] = ok ? __ldcg(ml + r) : -CUDART_INF_F;
+      le[u] = ok ? __ldcg(es + r) : 0.f;
 #pragma unroll
       for (int k = 0; k < 2; ++k)
-        if (k < per_lane)
-          v[u][k] = __ldcg(reinterpret_cast<const float4 *>(tmp + (size_t)r * D + 4 * lpr * k));
+        v[u][k] = (ok && k < per_lane)
+                      ? __ldcg(reinterpret_cast<const float4 *>(tmp + (size_t)r * D + 4 * lpr * k))
+                      : make_float4(0.f, 0.f, 0.f, 0.f);
     }
+    float M = acc.m;
 #pragma unroll
-    for (int u = 0; u < 4; ++u)
-#pragma unroll
-      for (int k = 0; k < 2; ++k)
-        if (k < per_lane) {
-          acc[k].x = fmaf(w[u], v[u][k].x, acc[k].x);
-          acc[k].y = fmaf(w[u], v[u][k].y, acc[k].y);
-          acc[k].z = fmaf(w[u], v[u][k].z, acc[k].z);
-          acc[k].w = fmaf(w[u], v[u][k].w, acc[k].w);
-        }
-  }
-  for (; i < np; i += stride) {
-    const float w = expf(__ldcg(ml + i) - mx) * __ldcg(es + i);
-#pragma unroll
-    for (int k = 0; k < 2; ++k)
-      if (k < per_lane) {
-        const float4 v = __ldcg(reinterpret_cast<const float4 *>(tmp + (size_t)i * D + 4 * lpr * k));
-        acc[k].x = fmaf(w, v.x, acc[k].x);
-        acc[k].y = fmaf(w, v.y, acc[k].y);
-        acc[k].z = fmaf(w, v.z, acc[k].z);
-        acc[k].w = fmaf(w, v.w, acc[k].w);
-      }
-  }
-  // fold the rows handled by different lane groups of the warp
-  for (int off = lpr; off < 32; off <<= 1)
+    for (int u = 0; u < 4; ++u) M = fmaxf(M, lm[u]);
+    const float f = acc.m == -CUDART_INF_F ? 0.f : expf(acc.m - M);
+    acc.S *= f;
 #pragma unroll
     for (int k = 0; k < 2; ++k) {
-      acc[k].x += __shfl_xor_sync(0xffffffffu, acc[k].x, off);
-      acc[k].y += __shfl_xor_sync(0xffffffffu, acc[k].y, off);
-      acc[k].z += __shfl_xor_sync(0xffffffffu, acc[k].z, off);
-      acc[k].w += __shfl_xor_sync(0xffffffffu, acc[k].w, off);
+      acc.a[k].x *= f;
+      acc.a[k].y *= f;
+      acc.a[k].z *= f;
+      acc.a[k].w *= f;
     }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const float w = lm[u] == -CUDART_INF_F ? 0.f : expf(lm[u] - M) * le[u];
+      acc.S += w;
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        acc.a[k].x = fmaf(w, v[u][k].x, acc.a[k].x);
+        acc.a[k].y = fmaf(w, v[u][k].y, acc.a[k].y);
+        acc.a[k].z = fmaf(w, v[u][k].z, acc.a[k].z);
+        acc.a[k].w = fmaf(w, v[u][k].w, acc.a[k].w);
+      }
+    }
+    acc.m = M;
+  }
+  // merge the row groups of the warp (lanes with the same column chunk)
+  for (int off = lpr; off < 32; off <<= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, acc.m, off);
+    const float S2 = __shfl_xor_sync(0xffffffffu, acc.S, off);
+    float4 a2[2];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      a2[k].x = __shfl_xor_sync(0xffffffffu, acc.a[k].x, off);
+      a2[k].y = __shfl_xor_sync(0xffffffffu, acc.a[k].y, off);
+      a2[k].z = __shfl_xor_sync(0xffffffffu, acc.a[k].z, off);
+      a2[k].w = __shfl_xor_sync(0xffffffffu, acc.a[k].w, off);
+    }
+    lse_merge(acc, m2, S2, a2, 2);
+  }
+  // merge the warps of the group
   if (wph > 1) {
     if (sub == 0) {
 #pragma unroll
       for (int k = 0; k < 2; ++k)
-        if (k < per_lane) part_sum[warp][cl + lpr * k] = acc[k];
+        if (k < per_lane) part_a[warp][cl + lpr * k] = acc.a[k];
+      if (lane == 0) {
+        part_m[warp] = acc.m;
+        part_S[warp] = acc.S;
+      }
     }
     __syncthreads();
     if (wig != 0) return;
-    if (sub == 0) {
+    if (sub == 0)
+      for (int w2 = 1; w2 < wph; ++w2) {
+        float4 a2[2];
 #pragma unroll
-      for (int k = 0; k < 2; ++k)
-        if (k < per_lane)
-          for (int w2 = 1; w2 < wph; ++w2) {
-            const float4 t = part_sum[warp + w2][cl + lpr * k];
-            acc[k].x += t.x;
-            acc[k].y += t.y;
-            acc[k].z += t.z;
-            acc[k].w += t.w;
-          }
-    }
+        for (int k = 0; k < 2; ++k)
+          a2[k] = k < per_lane ? part_a[warp + w2][cl + lpr * k] : make_float4(0.f, 0.f, 0.f, 0.f);
+        lse_merge(acc, part_m[warp + w2], part_S[warp + w2], a2, per_lane);
+      }
   }
   if (!live || sub != 0) return;
-  const float inv = np > 0 ? 1.f / wsum : 0.f;  // np == 0: empty sequence -> zeros
+  OutT *out = static_cast<OutT *>(p.out) + ((size_t)s * p.num_heads + h) * D + col0;
+  const float inv = np > 0 ? 1.f / acc.S : 0.f;  // np == 0: empty sequence -> zeros
 #pragma unroll
   for (int k = 0; k < 2; ++k)
     if (k < per_lane) {
       OutT *o = out + 4 * (cl + lpr * k);
-      o[0] = from_float<OutT>(acc[k].x * inv);
-      o[1] = from_float<OutT>(acc[k].y * inv);
-      o[2] = from_float<OutT>(acc[k].z * inv);
-      o[3] = from_float<OutT>(acc[k].w * inv);
+      o[0] = from_float<OutT>(acc.a[k].x * inv);
+      o[1] = from_float<OutT>(acc.a[k].y * inv);
+      o[2] = from_float<OutT>(acc.a[k].z * inv);
+      o[3] = from_float<OutT>(acc.a[k].w * inv);
     }
 }
 
