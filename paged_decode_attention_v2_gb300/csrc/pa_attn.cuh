@@ -549,7 +549,9 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) __maxnreg__((kernel_max_regs
       // ---- locate the item: (s, kvh, part, L)
       int s = 0, kvh = 0, part = 0, L = 0;
       bool found = false;
-      if (!p.write_partials) {  // V1: Hkv items per sequence, empty ones too
+      if (item < 0) {  // a corrupted work counter: stop rather than guess
+        if (lane == 0) report(p.status, kStatusBadInput);
+      } else if (!p.write_partials) {  // V1: Hkv items per sequence, empty ones too
         s = item / p.num_kv_heads;
         if (s < p.num_seqs) {
           found = true;
@@ -615,7 +617,9 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) __maxnreg__((kernel_max_regs
       // and win0+32+j (nxt); it slides by 32 pages when a stage reaches nxt.
       const int32_t *bt = p.block_tables + (size_t)s * p.max_blocks_per_seq;
       const int last_page = (tok_end - 1) >> p.log2_block_size;
-      auto load_entry = [&](int page) -> int { return page <= last_page ? __ldg(bt + page) : -1; };
+      auto load_entry = [&](int page) -> int {
+        return (page >= 0 && page <= last_page) ? __ldg(bt + page) : -1;
+      };
       int win0 = tok_begin >> p.log2_block_size;
       int cur = load_entry(win0 + lane);
       int nxt = load_entry(win0 + 32 + lane);
