@@ -191,10 +191,10 @@ def recorded_traffic(workload: str, kernel: str):
     return rec.get("dram_bytes_per_launch")
 
 
-def algorithmic_bytes(case, v2: bool) -> dict:
+def algorithmic_bytes(case, phase2_separate: bool) -> dict:
     """Bytes the dominant kernel must move: K and V of every token, the
-    queries, the block-table entries it dereferences and seq_lens; V1 also
-    writes the output (V2's Phase 1 writes only workspace partials, which are
+    queries, the block-table entries it dereferences and seq_lens, and the
+    output unless a separate Phase 2 kernel writes it (workspace partials are
     implementation overhead and not counted)."""
     elt = case.query.element_size()
     kv = case.kv_bytes()
@@ -202,7 +202,7 @@ def algorithmic_bytes(case, v2: bool) -> dict:
     pages = int(((case.seq_lens.to(torch.int64) + case.block_size - 1)
                  // case.block_size).sum().item())
     table = pages * 4 + case.num_seqs * 4
-    out = 0 if v2 else q
+    out = 0 if phase2_separate else q
     return {"kv": kv, "kernel": kv + q + table + out}
 
 
@@ -235,7 +235,10 @@ class Runner:
                                               self.max_seq_len, case.partition_size, sm))
         else:
             self.is_v2 = self.variant == pa.PA_VARIANT_V2
-        self.kernels_per_step = 2 if self.is_v2 else 1
+        # V2 sequences of at most 16 partitions get their combine inside the
+        # Phase 1 kernel; a Phase 2 kernel runs only if longer ones can occur.
+        self.has_phase2 = self.is_v2 and -(-self.max_seq_len // case.partition_size) > 16
+        self.kernels_per_step = 2 if self.has_phase2 else 1
 
     def step(self, q=None, bt=None, sl=None, out=None, phase1_event=None):
         self.pa.pa_forward(out if out is not None else self.out,
@@ -374,7 +377,7 @@ def run_ours(args):
     barrier(world)
     # per-kernel breakdown and end-to-end timing, still under load
     brk_steps = min(args.steps, 500)
-    brk_ms, phase1_ms = time_steps(runner, brk_steps, flush, with_phase=runner.is_v2)
+    brk_ms, phase1_ms = time_steps(runner, brk_steps, flush, with_phase=runner.has_phase2)
     e2e_ms, h2d, d2h = time_e2e(runner, min(args.steps, 500), flush)
     clocks = sampler.stop()
     runner.check_status()
@@ -389,10 +392,11 @@ def run_ours(args):
         return None
 
     peak, peak_kind = measured_hbm_peak()
-    alg = algorithmic_bytes(case, runner.is_v2)
+    alg = algorithmic_bytes(case, runner.has_phase2)
     dom_ms = statistics.mean(phase1_ms) if phase1_ms else statistics.mean(brk_ms)
     achieved = alg["kernel"] / (dom_ms / 1e3) / 1e9
-    kernel_name = "pa_attn_kernel(phase1)" if runner.is_v2 else "pa_attn_kernel(v1)"
+    kernel_name = ("pa_attn_kernel(phase1)" if runner.has_phase2 else
+                   "pa_attn_kernel(v2, combine fused)" if runner.is_v2 else "pa_attn_kernel(v1)")
     mean_ms = statistics.mean(step_ms)
     line = {
         "metric": METRIC,
@@ -447,7 +451,7 @@ def run_ours(args):
         r2 = Runner(sec, device, "auto", "auto", 0)
         for _ in range(max(args.warmup, 3)):
             r2.step()
-        ms2, p1 = time_steps(r2, min(args.steps, 500), flush, with_phase=r2.is_v2)
+        ms2, p1 = time_steps(r2, min(args.steps, 500), flush, with_phase=r2.has_phase2)
         r2.check_status()
         gbs = sec.kv_bytes() / (statistics.mean(ms2) / 1e3) / 1e9
         line["secondary"] = {SECONDARY: {

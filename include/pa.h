@@ -84,7 +84,10 @@ typedef struct {
                              stream between the Phase 1 and Phase 2 kernels
                              (lets a caller time the phases with events)   */
   int32_t ctas_per_sm;    /* persistent CTAs per SM, 0 = as many as fit     */
-  int32_t reserved;       /* 0                                              */
+  int32_t fuse_partitions;/* V2: sequences of at most this many partitions
+                             get the cross-partition combine inside the
+                             Phase 1 kernel; 0 = library default (16, the
+                             most), negative = never (Phase 2 kernel only) */
 } pa_options_t;
 
 /* Debug: every consumer warp waits on a barrier that nothing ever releases,
@@ -94,27 +97,28 @@ typedef struct {
 #define PA_DEBUG_STALL_CONSUMERS 1
 
 /* Bytes of workspace that pa_v2_forward needs (V1 needs only the 256-byte
- * status block; so does V2 for max_seq_len == 0).  Layout, each part
- * 256-byte aligned, in this order:
+ * status block).  Layout, each part 256-byte aligned, in this order:
  *   status      int32 status word + work-queue counters (a 256-byte block)
  *   max_logits  f32 [num_seqs][num_heads][max_parts]   Phase 1 max logit
  *   exp_sums    f32 [num_seqs][num_heads][max_parts]   sum exp(logit - max)
  *   tmp_out     f32 [num_seqs][num_heads][max_parts][head_size]  normalised
+ *   counters    int32 [num_seqs][num_heads]: partitions finished per
+ *               (sequence, KV head), for the fused cross-partition combine
  * with max_parts = ceil(max_seq_len / partition_size).  Returns 0 on bad
  * arguments. */
 size_t pa_workspace_bytes(int num_seqs, int num_heads, int head_size,
                           int max_seq_len, int partition_size);
 
-/* Byte offsets of the four workspace parts above (offsets[0..3]); returns
+/* Byte offsets of the five workspace parts above (offsets[0..4]); returns
  * PA_ERR_INVALID_ARG on bad arguments.  Lets callers read Phase 1 results. */
 pa_status_t pa_workspace_layout(int num_seqs, int num_heads, int head_size,
                                 int max_seq_len, int partition_size,
-                                size_t offsets[4]);
+                                size_t offsets[5]);
 
-/* Zero the status block of a new workspace (enqueued on `stream`).  Call
- * once after allocating it.  The block holds the status word, which kernels
- * only ever set to a nonzero code, and the work-queue counters of the
- * attention kernel, which every launch leaves at zero when it finishes. */
+/* Zero a new workspace (enqueued on `stream`).  Call once after allocating
+ * it, and again after a call reported a device error.  Kernels only ever
+ * set the status word to a nonzero code; the work-queue and combine
+ * counters are left at zero by every launch that completes. */
 pa_status_t pa_workspace_init(void *workspace, size_t workspace_bytes,
                               void *stream);
 
@@ -131,10 +135,13 @@ pa_status_t pa_v1_forward(void *out, const void *query, const void *key_cache,
                           int dtype, void *workspace, size_t workspace_bytes,
                           void *stream);
 
-/* V2: Phase 1 kernel with one CTA per (sequence, KV head, partition), writing
- * max_logits / exp_sums / tmp_out into the workspace, then the Phase 2
- * log-sum-exp reduce kernel writing out.  Same arguments as V1; the
- * workspace must hold pa_workspace_bytes(...) bytes. */
+/* V2: the Phase 1 kernel computes every (sequence, KV head, partition) and
+ * writes max_logits / exp_sums / tmp_out into the workspace; then the
+ * log-sum-exp combine writes out.  For a sequence of at most 16 partitions
+ * (pa_options_t.fuse_partitions) the last Phase 1 work item of each
+ * (sequence, KV head) does that combine; a Phase 2 kernel does it for longer
+ * sequences and is launched only if max_seq_len allows one.  Same arguments
+ * as V1; the workspace must hold pa_workspace_bytes(...) bytes. */
 pa_status_t pa_v2_forward(void *out, const void *query, const void *key_cache,
                           const void *value_cache, const int32_t *block_tables,
                           const int32_t *seq_lens, int num_seqs, int num_heads,

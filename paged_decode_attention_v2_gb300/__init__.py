@@ -55,7 +55,7 @@ class pa_options_t(ctypes.Structure):
     _fields_ = [("variant", ctypes.c_int32), ("math", ctypes.c_int32),
                 ("num_stages", ctypes.c_int32), ("debug_flags", ctypes.c_int32),
                 ("wait_limit_ns", ctypes.c_uint64), ("phase1_event", ctypes.c_void_p),
-                ("ctas_per_sm", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+                ("ctas_per_sm", ctypes.c_int32), ("fuse_partitions", ctypes.c_int32)]
 
 
 _lib = None
@@ -144,8 +144,8 @@ def pa_workspace_bytes(num_seqs: int, num_heads: int, head_size: int, max_seq_le
 
 
 def pa_workspace_layout(num_seqs: int, num_heads: int, head_size: int, max_seq_len: int,
-                        partition_size: int) -> tuple[int, int, int, int]:
-    off = (ctypes.c_size_t * 4)()
+                        partition_size: int) -> tuple[int, int, int, int, int]:
+    off = (ctypes.c_size_t * 5)()
     _check(load_library().pa_workspace_layout(num_seqs, num_heads, head_size, max_seq_len,
                                               partition_size, off), "pa_workspace_layout")
     return tuple(int(x) for x in off)
@@ -213,7 +213,7 @@ def pa_v2_forward_noalloc(out, query, key_cache, value_cache, block_tables, seq_
 def pa_forward(out, query, key_cache, value_cache, block_tables, seq_lens, scale,
                partition_size, workspace, max_seq_len=None, stream=None, variant=PA_VARIANT_AUTO,
                math=PA_MATH_AUTO, num_stages=0, debug_flags=0, wait_limit_ns=0,
-               phase1_event=None, ctas_per_sm=0) -> None:
+               phase1_event=None, ctas_per_sm=0, fuse_partitions=0) -> None:
     """V1 or V2 chosen by pa_choose_v2, or forced through the options.
     ``phase1_event`` (a torch.cuda.Event) is recorded between V2's two kernels."""
     ev = 0
@@ -222,7 +222,8 @@ def pa_forward(out, query, key_cache, value_cache, block_tables, seq_lens, scale
         if not ev:
             raise ValueError("phase1_event has no CUDA event yet (torch creates it at the "
                              "first record(); record it once before passing it)")
-    opts = pa_options_t(variant, math, num_stages, debug_flags, wait_limit_ns, ev, ctas_per_sm, 0)
+    opts = pa_options_t(variant, math, num_stages, debug_flags, wait_limit_ns, ev, ctas_per_sm,
+                        fuse_partitions)
     _check(load_library().pa_forward(*_fwd_args(
         out, query, key_cache, value_cache, block_tables, seq_lens, scale, partition_size,
         workspace, max_seq_len, stream), ctypes.byref(opts)), "pa_forward")

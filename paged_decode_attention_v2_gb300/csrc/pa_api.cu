@@ -286,7 +286,7 @@ pa_status_t launch(const Call &c, bool v2, const pa_options_t &opt) {
 
   uint8_t *ws = static_cast<uint8_t *>(c.workspace);
   const int max_parts = v2 ? max_parts_of(c.max_seq_len, c.partition_size) : 1;
-  size_t off[4] = {0, 0, 0, 0};
+  size_t off[5] = {0, 0, 0, 0, 0};
   if (v2) {
     if (pa_workspace_layout(c.num_seqs, c.num_heads, c.head_size, c.max_seq_len,
                             c.partition_size, off) != PA_OK)
@@ -320,6 +320,12 @@ pa_status_t launch(const Call &c, bool v2, const pa_options_t &opt) {
   p.range_tokens = v2 ? c.partition_size : (c.max_seq_len > 0 ? c.max_seq_len : 1);
   p.max_parts = max_parts > 0 ? max_parts : 1;
   p.write_partials = v2 ? 1 : 0;
+  if (v2) {
+    int fuse = opt.fuse_partitions == 0 ? kFuseLimitMax
+                                        : (opt.fuse_partitions < 0 ? 0 : opt.fuse_partitions);
+    p.fuse_limit = fuse > kFuseLimitMax ? kFuseLimitMax : fuse;
+    p.group_count = reinterpret_cast<int *>(ws + off[4]);
+  }
   p.num_stages = stages;
   p.debug_flags = opt.debug_flags;
   p.scale_log2 = (float)((double)c.scale * 1.4426950408889634);
@@ -351,6 +357,8 @@ pa_status_t launch(const Call &c, bool v2, const pa_options_t &opt) {
     if (e != cudaSuccess) return fail_cuda("launch attention kernel", e);
   }
   if (!v2) return PA_OK;
+  // Phase 2 has work only for sequences of more than fuse_limit partitions.
+  if (max_parts_of(c.max_seq_len, c.partition_size) <= p.fuse_limit) return PA_OK;
   if (opt.phase1_event) {
     cudaError_t e = cudaEventRecord(static_cast<cudaEvent_t>(opt.phase1_event), c.stream);
     if (e != cudaSuccess) return fail_cuda("cudaEventRecord(phase1_event)", e);
@@ -371,6 +379,7 @@ pa_status_t launch(const Call &c, bool v2, const pa_options_t &opt) {
   r.max_parts = p.max_parts;
   r.partition_size = c.partition_size;
   r.max_seq_len = c.max_seq_len;
+  r.fuse_limit = p.fuse_limit;
   // Warps per (sequence, head): enough that each warp's chain of dependent
   // tmp_out loads stays short; then split columns over CTAs until the grid
   // covers the GPU twice.
@@ -443,16 +452,15 @@ extern "C" {
 
 size_t pa_workspace_bytes(int num_seqs, int num_heads, int head_size, int max_seq_len,
                           int partition_size) {
-  size_t off[4];
+  size_t off[5];
   if (pa_workspace_layout(num_seqs, num_heads, head_size, max_seq_len, partition_size, off) !=
       PA_OK)
     return 0;
-  const size_t parts = (size_t)max_parts_of(max_seq_len, partition_size);
-  return off[3] + align256((size_t)num_seqs * num_heads * parts * head_size * 4);
+  return off[4] + align256((size_t)num_seqs * num_heads * 4);
 }
 
 pa_status_t pa_workspace_layout(int num_seqs, int num_heads, int head_size, int max_seq_len,
-                                int partition_size, size_t offsets[4]) {
+                                int partition_size, size_t offsets[5]) {
   if (!offsets || num_seqs < 0 || num_heads < 1 || head_size < 1 || max_seq_len < 0 ||
       partition_size < 1)
     return PA_ERR_INVALID_ARG;
@@ -462,14 +470,16 @@ pa_status_t pa_workspace_layout(int num_seqs, int num_heads, int head_size, int 
   offsets[1] = kStatusBytes;
   offsets[2] = offsets[1] + stats;
   offsets[3] = offsets[2] + stats;
+  offsets[4] = offsets[3] + align256((size_t)num_seqs * num_heads * parts * head_size * 4);
   return PA_OK;
 }
 
 pa_status_t pa_workspace_init(void *workspace, size_t workspace_bytes, void *stream) {
   if (!workspace || workspace_bytes < (size_t)kStatusBytes || !aligned(workspace, 256))
     return PA_ERR_INVALID_ARG;
-  cudaError_t e = cudaMemsetAsync(workspace, 0, kStatusBytes, static_cast<cudaStream_t>(stream));
-  if (e != cudaSuccess) return fail_cuda("cudaMemsetAsync(status)", e);
+  cudaError_t e =
+      cudaMemsetAsync(workspace, 0, workspace_bytes, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail_cuda("cudaMemsetAsync(workspace)", e);
   return PA_OK;
 }
 

@@ -56,8 +56,13 @@ struct StageInfo {
   int tok0;          // first token of the stage
   int tok_end;       // end of the item's token range
   int flags;         // kStage*
-  int pad[2];
+  int np;            // partitions of the item's sequence (V2)
+  int pad;
 };
+
+// Largest partition count whose cross-partition combine may run inside this
+// kernel: its scratch holds 3 floats per (head, partition).
+constexpr int kFuseCap = kFuseLimitMax;
 
 // Geometry of one K (or V) stage buffer as TMA writes it:
 //   [unit][panel][unit_rows][128 bytes]
@@ -480,7 +485,10 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) __maxnreg__((kernel_max_regs
   // The consumer warps merge their states in the K/V bytes of an item's last
   // stage when they fit (the data is dead by then; the slot is released after
   // the merge), else in a dedicated area.
-  constexpr int MERGE_BYTES = NW * GMAX * (D + 4) * 4 + NW * GMAX * 2 * 4;
+  constexpr int MERGE_BYTES_STATE = NW * GMAX * (D + 4) * 4 + NW * GMAX * 2 * 4;
+  constexpr int MERGE_BYTES_FUSE = (3 * GMAX * kFuseCap + 4) * 4;  // fused combine scratch
+  constexpr int MERGE_BYTES =
+      MERGE_BYTES_STATE > MERGE_BYTES_FUSE ? MERGE_BYTES_STATE : MERGE_BYTES_FUSE;
   constexpr bool MERGE_IN_SLOT = MERGE_BYTES <= 2 * HALF_BYTES;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -547,7 +555,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) __maxnreg__((kernel_max_regs
     int item = blockIdx.x;
     while (true) {
       // ---- locate the item: (s, kvh, part, L)
-      int s = 0, kvh = 0, part = 0, L = 0;
+      int s = 0, kvh = 0, part = 0, L = 0, np_s = 1;
       bool found = false;
       if (item < 0) {  // a corrupted work counter: stop rather than guess
         if (lane == 0) report(p.status, kStatusBadInput);
@@ -574,7 +582,13 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) __maxnreg__((kernel_max_regs
                 c_L = c_L < 0 ? 0 : p.max_seq_len;
               }
             }
-            c_cnt = p.num_kv_heads * ((c_L + p.range_tokens - 1) / p.range_tokens);
+            // With the cross-partition combine fused into this kernel, an
+            // empty sequence gets one item per KV head that writes zeros;
+            // lanes past the last sequence count none.
+            const int c_np = (c_L + p.range_tokens - 1) / p.range_tokens;
+            c_cnt = sl >= p.num_seqs
+                        ? 0
+                        : p.num_kv_heads * (c_np == 0 && p.fuse_limit > 0 ? 1 : c_np);
             c_incl = c_cnt;
 #pragma unroll
             for (int off = 1; off < 32; off <<= 1) {
@@ -590,10 +604,11 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) __maxnreg__((kernel_max_regs
             s = cs + ls;
             L = __shfl_sync(0xffffffffu, c_L, ls);
             const int first = cbase + __shfl_sync(0xffffffffu, c_incl - c_cnt, ls);
-            const int np = (L + p.range_tokens - 1) / p.range_tokens;
-            kvh = (item - first) / np;
-            part = (item - first) % np;
-            found = true;
+            np_s = (L + p.range_tokens - 1) / p.range_tokens;
+            const int items_per_head = np_s > 0 ? np_s : 1;
+            kvh = (item - first) / items_per_head;
+            part = (item - first) % items_per_head;
+            found = s < p.num_seqs;  // always, by the count above; never write past the batch
             break;
           }
           if (cs + 32 >= p.num_seqs) break;
@@ -607,7 +622,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) __maxnreg__((kernel_max_regs
 
       const int tok_begin = part * p.range_tokens;
       const int tok_end = min(tok_begin + p.range_tokens, L);
-      if (tok_end <= tok_begin) {  // V1, empty sequence: zeros
+      if (tok_end <= tok_begin) {  // empty sequence (V1, or V2 with the fused combine): zeros
         T *o = static_cast<T *>(p.out) + ((size_t)s * p.num_heads + (size_t)kvh * p.group) * D;
         for (int e = lane; e < p.group * D; e += 32) o[e] = from_float<T>(0.f);
         item = grab_value(next_raw);
@@ -657,6 +672,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) __maxnreg__((kernel_max_regs
           h.tok0 = stage_tok0;
           h.tok_end = tok_end;
           h.flags = (first ? kStageFirst : 0) | (j == n_st - 1 ? kStageLast : 0);
+          h.np = np_s;
           mbar_arrive_expect_tx(full0 + 8 * st, (uint32_t)__popc(valid_mask) * U * ROW_BYTES * 2 +
                                                     (first ? (uint32_t)qbytes : 0u));
         }
@@ -803,6 +819,79 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) __maxnreg__((kernel_max_regs
           o[1] = from_float<T>(acc.y);
           o[2] = from_float<T>(acc.z);
           o[3] = from_float<T>(acc.w);
+        }
+      }
+      if (p.write_partials && h.np <= p.fuse_limit) {
+        // Phase 2 inside Phase 1 for a sequence of few partitions: the last
+        // CTA to finish one of them (per KV head) combines them all, with the
+        // same log-sum-exp rule as the Phase 2 kernel.
+        __threadfence();  // this partition's partials are visible device-wide
+        ok = cons_sync();
+        if (!ok) break;
+        int *cnt = p.group_count + (size_t)h.s * p.num_kv_heads + h.kvh;
+        volatile int *last = reinterpret_cast<volatile int *>(mb);
+        if (threadIdx.x == 0) {
+          // The barrier above ordered every consumer thread's partial writes
+          // before this point; the fence and the acq_rel increment publish
+          // them device-wide to the CTA that finds the final count.
+          __threadfence();
+          *last = atomic_add_acq_rel_gpu(cnt, 1) == h.np - 1 ? 1 : 0;
+        }
+        ok = cons_sync();
+        if (!ok) break;
+        if (*last) {
+          __threadfence();  // the other CTAs' partials are visible to our reads
+          const int np = h.np;
+          float *mlv = reinterpret_cast<float *>(mb) + 4;  // [G][np]
+          float *wts = mlv + GMAX * kFuseCap;              // [G][np]
+          float *esv = wts + GMAX * kFuseCap;              // [G][np]
+          for (int k = threadIdx.x; k < G * np; k += NCONS) {
+            const size_t r = (head0 + k / np) * p.max_parts + k % np;
+            mlv[k] = __ldcg(p.max_logits + r);
+            esv[k] = __ldcg(p.exp_sums + r);
+          }
+          ok = cons_sync();
+          if (!ok) break;
+          for (int hh = threadIdx.x; hh < G; hh += NCONS) {
+            float M = -CUDART_INF_F;
+            for (int j = 0; j < np; ++j) M = fmaxf(M, mlv[hh * np + j]);
+            float sum = 0.f;
+            for (int j = 0; j < np; ++j) {
+              const float r = esv[hh * np + j] * expf(mlv[hh * np + j] - M);
+              wts[hh * np + j] = r;
+              sum += r;
+            }
+            const float inv = 1.f / sum;
+            for (int j = 0; j < np; ++j) wts[hh * np + j] *= inv;
+          }
+          ok = cons_sync();
+          if (!ok) break;
+          for (int idx = threadIdx.x; idx < G * (D / 4); idx += NCONS) {
+            const int hh = idx / (D / 4), d = 4 * (idx % (D / 4));
+            const float *src = p.tmp_out + (head0 + hh) * p.max_parts * D + d;
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int j = 0; j < np; j += 4) {
+              float4 v[4];
+#pragma unroll
+              for (int u = 0; u < 4; ++u)
+                v[u] = j + u < np ? __ldcg(reinterpret_cast<const float4 *>(src + (size_t)(j + u) * D))
+                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                const float w = j + u < np ? wts[hh * np + j + u] : 0.f;
+                acc.x = fmaf(w, v[u].x, acc.x);
+                acc.y = fmaf(w, v[u].y, acc.y);
+                acc.z = fmaf(w, v[u].z, acc.z);
+                acc.w = fmaf(w, v[u].w, acc.w);
+              }
+            }
+            T *o = static_cast<T *>(p.out) + (head0 + hh) * D + d;
+            o[0] = from_float<T>(acc.x);
+            o[1] = from_float<T>(acc.y);
+            o[2] = from_float<T>(acc.z);
+            o[3] = from_float<T>(acc.w);
+          }
+          if (threadIdx.x == 0) *cnt = 0;  // ready for the next launch
         }
       }
       if (MERGE_IN_SLOT) {

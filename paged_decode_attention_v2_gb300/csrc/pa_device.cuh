@@ -116,6 +116,19 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Device-scope counter increment with acquire-release ordering: the
+// caller's earlier writes (and those it has observed) are visible to whoever
+// reads the new value, and writes published before the old value are
+// visible to the caller afterwards.
+__device__ __forceinline__ int atomic_add_acq_rel_gpu(int *addr, int v) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;"
+               : "=r"(old)
+               : "l"(addr), "r"(v)
+               : "memory");
+  return old;
+}
+
 // Programmatic dependent launch: let the next kernel in the stream start its
 // prologue; it waits for this grid's completion before reading our results.
 __device__ __forceinline__ void pdl_launch_dependents() {

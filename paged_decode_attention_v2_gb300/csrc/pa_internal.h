@@ -12,6 +12,7 @@ constexpr int kPanelBytes = 128;    // TMA box width: one 128-byte swizzle span
 constexpr int kStatusBytes = 256;   // status block at the head of the workspace
 constexpr uint64_t kDefaultWaitLimitNs = 1000000000ull;  // 1 s
 constexpr uint64_t kDrainLimitNs = 1000000000ull;        // drain of own copies
+constexpr int kFuseLimitMax = 16;  // most partitions a fused combine handles
 
 // Parameters of the attention kernel (Phase 1 of V2, or V1).
 struct AttnParams {
@@ -31,6 +32,9 @@ struct AttnParams {
   int range_tokens;   // tokens per work item: partition_size (V2) or max_seq_len (V1)
   int max_parts;      // partitions per (seq, head) in the workspace layout
   int write_partials; // 1: V2 Phase 1 outputs, 0: V1 final output
+  int fuse_limit;     // V2: sequences of at most this many partitions get the
+                      // cross-partition combine inside this kernel (0 = none)
+  int *group_count;   // V2 fused combine: finished partitions per (seq, kv head)
   int num_stages;
   int debug_flags;
   float scale_log2;   // scale * log2(e)
@@ -44,6 +48,8 @@ struct ReduceParams {
   const int32_t *seq_lens;
   int *status;
   int num_seqs, num_heads, head_size, max_parts, partition_size, max_seq_len;
+  int fuse_limit;      // sequences of at most this many partitions were
+                       // finished by Phase 1 (0 = none)
   int cols_per_cta;    // head_size / gridDim.y
   int warps_per_head;  // 1, 2, 4 or 8 warps share one (sequence, head)
 };
@@ -68,6 +74,8 @@ inline size_t attn_smem_bytes(int head_size, int elt, int consumer_warps, int ma
   size_t qslots = (size_t)max_group * head_size * elt * stages;
   size_t merge = (size_t)consumer_warps * max_group * (head_size + 4) * 4 +
                  (size_t)consumer_warps * max_group * 2 * 4;
+  const size_t fuse_scratch = (3 * (size_t)max_group * kFuseLimitMax + 4) * 4;
+  if (merge < fuse_scratch) merge = fuse_scratch;
   if (merge <= stage) merge = 0;  // merged inside the item's last stage
   size_t headers = 32 * (size_t)stages;
   size_t bars = 8 * (2 * (size_t)stages + 2);  // full, empty, never-set, consumer barrier

@@ -63,11 +63,18 @@ extern "C" pa_status_t pa_v2_forward_noalloc(
   void *scratch = nullptr;
   pa_status_t st = scratch_for_current_device(&scratch);
   if (st != PA_OK) return st;
-  // The array keeps whatever the previous call left in it.  Only the status
-  // word must start at zero; the partials are written before they are read.
+  // The array keeps whatever the previous call left in it.  The status block
+  // and the combine counters must start at zero; the partials are written
+  // before they are read.
+  size_t off[5];
+  if (pa_workspace_layout(num_seqs, num_heads, head_size, max_seq_len, partition_size, off) !=
+      PA_OK)
+    return PA_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (num_seqs > 0 &&
-      cudaMemsetAsync(scratch, 0, pa::kStatusBytes, static_cast<cudaStream_t>(stream)) !=
-          cudaSuccess)
+      (cudaMemsetAsync(scratch, 0, pa::kStatusBytes, s) != cudaSuccess ||
+       cudaMemsetAsync(static_cast<unsigned char *>(scratch) + off[4], 0,
+                       (size_t)num_seqs * num_heads * sizeof(int), s) != cudaSuccess))
     return PA_ERR_CUDA;
   return pa_v2_forward(out, query, key_cache, value_cache, block_tables, seq_lens, num_seqs,
                        num_heads, num_kv_heads, head_size, num_blocks, block_size,

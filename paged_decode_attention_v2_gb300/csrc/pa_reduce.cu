@@ -67,10 +67,17 @@ __global__ void __launch_bounds__(kReduceThreads)
   const int col0 = blockIdx.y * ncols;
 
   int np = 0;
+  bool done = !live;  // sequences that Phase 1 finished are left alone
   if (live) {
     int L = p.seq_lens[s];
     L = L < 0 ? 0 : (L > p.max_seq_len ? p.max_seq_len : L);  // Phase 1 reported it
     np = (L + p.partition_size - 1) / p.partition_size;
+    // With the combine fused (fuse_limit > 0) Phase 1 also wrote the zeros
+    // of empty sequences; without it, this kernel writes them.
+    if (p.fuse_limit > 0 && np <= p.fuse_limit) {
+      done = true;
+      np = 0;
+    }
   }
   const size_t row0 = ((size_t)s * p.num_heads + h) * p.max_parts;
   const float *ml = p.max_logits + row0;
@@ -166,7 +173,7 @@ __global__ void __launch_bounds__(kReduceThreads)
         lse_merge(acc, part_m[warp + w2], part_S[warp + w2], a2, per_lane);
       }
   }
-  if (!live || sub != 0) return;
+  if (done || sub != 0) return;
   OutT *out = static_cast<OutT *>(p.out) + ((size_t)s * p.num_heads + h) * D + col0;
   const float inv = np > 0 ? 1.f / acc.S : 0.f;  // np == 0: empty sequence -> zeros
 #pragma unroll

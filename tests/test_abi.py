@@ -58,10 +58,11 @@ def test_workspace_layout_and_size(lib):
     stats = B * H * parts * 4
     assert off[2] - off[1] >= stats and off[2] - off[1] < stats + 256
     assert off[3] - off[2] == off[2] - off[1]
+    assert len(off) == 5 and off[4] - off[3] >= B * H * parts * D * 4
     size = pa.pa_workspace_bytes(B, H, D, L, P)
-    assert size >= off[3] + B * H * parts * D * 4 and size % 256 == 0
-    # no partitions: status block only
-    assert pa.pa_workspace_bytes(4, 8, 64, 0, 512) == 256
+    assert size >= off[4] + B * H * 4 and size % 256 == 0
+    # no partitions: the status block and the combine counters
+    assert pa.pa_workspace_bytes(4, 8, 64, 0, 512) == 256 + 256
     assert pa.pa_workspace_bytes(-1, 8, 64, 10, 512) == 0
     assert pa.pa_workspace_bytes(1, 8, 64, 10, 0) == 0
 
@@ -90,7 +91,7 @@ def _call(lib, variant=pa.PA_VARIANT_V2, **over):
              scale=0.1, partition_size=512, dtype=pa.PA_DTYPE_BF16, workspace=FAKE,
              workspace_bytes=1 << 30, stream=0)
     a.update(over)
-    opts = pa.pa_options_t(variant, 0, 0, 0, 0, None)
+    opts = pa.pa_options_t(variant, 0, 0, 0, 0, None, 0, 0)
     return lib.pa_forward(a["out"], a["query"], a["key_cache"], a["value_cache"],
                           a["block_tables"], a["seq_lens"], a["num_seqs"], a["num_heads"],
                           a["num_kv_heads"], a["head_size"], a["num_blocks"], a["block_size"],

@@ -107,3 +107,51 @@ def test_one_hot_logit_selects_one_value():
     out = DeviceCase(case).run(variant=pa.PA_VARIANT_V2)
     v = case.value_cache[blk, 0, 1234 % 16]
     assert torch.equal(out[0].cpu(), v.expand(8, -1))
+
+
+def test_fused_combine_reads_every_partition():
+    """Regression: the CTA that finishes a sequence's last partition must see
+    every other CTA's partials.  A bf16 batch warms the GPU first (the
+    failure showed with that timing); then a 4-partition f32 sequence runs
+    through the fused combine repeatedly and must match the oracle to 1e-5."""
+    warm = workloads.make_case("warm", 7, 3, 16, 2, 128, torch.bfloat16, 16, [1, 700, 1300],
+                               partition_size=512, extra_blocks=4)
+    DeviceCase(warm).run(variant=pa.PA_VARIANT_V2)
+    case = workloads.make_case("fused", 8, 2, 4, 1, 64, torch.float32, 16, [37, 1000],
+                               partition_size=256, extra_blocks=2)
+    ref = reference(case)
+    dc = DeviceCase(case)
+    for _ in range(8):
+        assert_close(dc.run(variant=pa.PA_VARIANT_V2), ref, torch.float32, "fused combine")
+
+
+@pytest.mark.parametrize("fuse", [0, -1])
+@pytest.mark.parametrize("dtype,H,Hkv,D", [(torch.float32, 4, 1, 64), (torch.bfloat16, 16, 2, 128)])
+def test_writes_stay_inside_out_and_workspace(dtype, H, Hkv, D, fuse):
+    """Regression: every write lands inside `out` and the workspace.  Both are
+    views at the head of larger buffers whose tails hold a canary, and the
+    inputs are unchanged afterwards.  The batch has fewer sequences than a
+    warp scans at once and an empty one."""
+    lens = [0, 37, 1000]
+    case = workloads.make_case("bounds", 91, len(lens), H, Hkv, D, dtype, 16, lens,
+                               partition_size=256, extra_blocks=2)
+    ref = reference(case)
+    host = [case.query, case.key_cache, case.value_cache, case.block_tables, case.seq_lens]
+    q, kc, vc, bt, sl = (t.cuda() for t in host)
+    canary = 1 << 16
+    nbytes = pa.pa_workspace_bytes(case.num_seqs, H, D, case.max_seq_len, 256)
+    wsbuf = torch.full((nbytes + canary,), 0xAB, dtype=torch.uint8, device="cuda")
+    ws = wsbuf[:nbytes]
+    pa.pa_workspace_init(ws)
+    n = case.query.numel()
+    for variant in (pa.PA_VARIANT_V1, pa.PA_VARIANT_V2):
+        obuf = torch.full((n + canary,), float("nan"), dtype=dtype, device="cuda")
+        out = obuf[:n].view(case.query.shape)
+        pa.pa_forward(out, q, kc, vc, bt, sl, case.scale, 256, ws, max_seq_len=case.max_seq_len,
+                      variant=variant, fuse_partitions=fuse)
+        assert pa.pa_read_device_status(ws) == pa.PA_OK
+        assert_close(out, ref, dtype, f"v{variant}")
+        assert torch.all(torch.isnan(obuf[n:])), "write past the end of out"
+        assert torch.all(wsbuf[nbytes:] == 0xAB), "write past the end of the workspace"
+        for dev_t, host_t in zip((q, kc, vc, bt, sl), host):
+            assert torch.equal(dev_t.cpu(), host_t), "an input was modified"
