@@ -59,6 +59,9 @@ def parse_args(argv=None):
     ap.add_argument("--math", choices=["auto", "tensor", "simt"], default="auto")
     ap.add_argument("--stages", type=int, default=0)
     ap.add_argument("--ctas-per-sm", type=int, default=0)
+    ap.add_argument("--fuse-partitions", type=int, default=0,
+                    help="V2: combine sequences of at most this many partitions inside "
+                         "Phase 1 (0: never, the library default)")
     ap.add_argument("--partition-size", type=int, default=0)
     ap.add_argument("--no-secondary", action="store_true",
                     help="skip the extra long-context measurement")
@@ -209,7 +212,7 @@ def algorithmic_bytes(case, phase2_separate: bool) -> dict:
 class Runner:
     """A workload resident on the GPU plus the call that runs one step."""
 
-    def __init__(self, case, device, variant, math, stages, ctas_per_sm=0):
+    def __init__(self, case, device, variant, math, stages, ctas_per_sm=0, fuse_partitions=0):
         import paged_decode_attention_v2_gb300 as pa
         self.pa = pa
         self.case = case
@@ -227,6 +230,7 @@ class Runner:
                      "simt": pa.PA_MATH_SIMT}[math]
         self.stages = stages
         self.ctas_per_sm = ctas_per_sm
+        self.fuse_partitions = fuse_partitions
         self.ws = pa.alloc_workspace(case.num_seqs, case.num_heads, case.head_size,
                                      self.max_seq_len, case.partition_size, device=device)
         sm = torch.cuda.get_device_properties(device).multi_processor_count
@@ -235,9 +239,11 @@ class Runner:
                                               self.max_seq_len, case.partition_size, sm))
         else:
             self.is_v2 = self.variant == pa.PA_VARIANT_V2
-        # V2 sequences of at most 16 partitions get their combine inside the
-        # Phase 1 kernel; a Phase 2 kernel runs only if longer ones can occur.
-        self.has_phase2 = self.is_v2 and -(-self.max_seq_len // case.partition_size) > 16
+        # With fusion asked for, V2 sequences of at most min(n, 16) partitions
+        # get their combine inside the Phase 1 kernel, and a Phase 2 kernel
+        # runs only if longer ones can occur.
+        fuse = min(fuse_partitions, 16) if fuse_partitions > 0 else 0
+        self.has_phase2 = self.is_v2 and -(-self.max_seq_len // case.partition_size) > fuse
         self.kernels_per_step = 2 if self.has_phase2 else 1
 
     def step(self, q=None, bt=None, sl=None, out=None, phase1_event=None):
@@ -248,7 +254,7 @@ class Runner:
                            self.case.scale, self.case.partition_size, self.ws,
                            max_seq_len=self.max_seq_len, variant=self.variant, math=self.math,
                            num_stages=self.stages, phase1_event=phase1_event,
-                           ctas_per_sm=self.ctas_per_sm)
+                           ctas_per_sm=self.ctas_per_sm, fuse_partitions=self.fuse_partitions)
 
     def check_status(self):
         st = self.pa.pa_read_device_status(self.ws)
@@ -362,7 +368,8 @@ def run_ours(args):
 
     P = args.partition_size or None
     case = workloads.config_case(args.workload, P, seed_offset=rank)
-    runner = Runner(case, device, args.variant, args.math, args.stages, args.ctas_per_sm)
+    runner = Runner(case, device, args.variant, args.math, args.stages, args.ctas_per_sm,
+                    args.fuse_partitions)
     flush = l2_flush_buffer(device)
     for _ in range(args.warmup):
         runner.step()
@@ -451,7 +458,12 @@ def run_ours(args):
         r2 = Runner(sec, device, "auto", "auto", 0)
         for _ in range(max(args.warmup, 3)):
             r2.step()
-        ms2, p1 = time_steps(r2, min(args.steps, 500), flush, with_phase=r2.has_phase2)
+        # the step as a whole (Phase 2 chained to Phase 1), then a second pass
+        # with an event between the phases for the split
+        ms2, _ = time_steps(r2, min(args.steps, 500), flush)
+        p1 = None
+        if r2.has_phase2:
+            _, p1 = time_steps(r2, min(args.steps, 200), flush, with_phase=True)
         r2.check_status()
         gbs = sec.kv_bytes() / (statistics.mean(ms2) / 1e3) / 1e9
         line["secondary"] = {SECONDARY: {

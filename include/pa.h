@@ -85,9 +85,9 @@ typedef struct {
                              (lets a caller time the phases with events)   */
   int32_t ctas_per_sm;    /* persistent CTAs per SM, 0 = as many as fit     */
   int32_t fuse_partitions;/* V2: sequences of at most this many partitions
-                             get the cross-partition combine inside the
-                             Phase 1 kernel; 0 = library default (16, the
-                             most), negative = never (Phase 2 kernel only) */
+                             (capped at 16) get the cross-partition combine
+                             inside the Phase 1 kernel; 0 (the default) or
+                             negative = never: the Phase 2 kernel does it */
 } pa_options_t;
 
 /* Debug: every consumer warp waits on a barrier that nothing ever releases,
@@ -137,10 +137,11 @@ pa_status_t pa_v1_forward(void *out, const void *query, const void *key_cache,
 
 /* V2: the Phase 1 kernel computes every (sequence, KV head, partition) and
  * writes max_logits / exp_sums / tmp_out into the workspace; then the
- * log-sum-exp combine writes out.  For a sequence of at most 16 partitions
- * (pa_options_t.fuse_partitions) the last Phase 1 work item of each
- * (sequence, KV head) does that combine; a Phase 2 kernel does it for longer
- * sequences and is launched only if max_seq_len allows one.  Same arguments
+ * log-sum-exp combine (Phase 2 kernel) writes out.  With
+ * pa_options_t.fuse_partitions = n > 0, for a sequence of at most min(n, 16)
+ * partitions the last Phase 1 work item of each (sequence, KV head) does
+ * that combine instead, and the Phase 2 kernel is launched only if
+ * max_seq_len allows a longer sequence.  Same arguments
  * as V1; the workspace must hold pa_workspace_bytes(...) bytes. */
 pa_status_t pa_v2_forward(void *out, const void *query, const void *key_cache,
                           const void *value_cache, const int32_t *block_tables,

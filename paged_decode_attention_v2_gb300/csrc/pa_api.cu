@@ -321,8 +321,9 @@ pa_status_t launch(const Call &c, bool v2, const pa_options_t &opt) {
   p.max_parts = max_parts > 0 ? max_parts : 1;
   p.write_partials = v2 ? 1 : 0;
   if (v2) {
-    int fuse = opt.fuse_partitions == 0 ? kFuseLimitMax
-                                        : (opt.fuse_partitions < 0 ? 0 : opt.fuse_partitions);
+    // Off unless asked for: on the workloads measured so far the separate
+    // Phase 2 kernel costs less than the per-item handshake of the fused one.
+    const int fuse = opt.fuse_partitions > 0 ? opt.fuse_partitions : 0;
     p.fuse_limit = fuse > kFuseLimitMax ? kFuseLimitMax : fuse;
     p.group_count = reinterpret_cast<int *>(ws + off[4]);
   }
@@ -352,13 +353,23 @@ pa_status_t launch(const Call &c, bool v2, const pa_options_t &opt) {
     cfg.blockDim = dim3((unsigned)threads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = c.stream;
+    // Programmatic dependent launch: the kernel's launch and shared-memory
+    // set-up overlap the tail of the previous kernel in the stream; the
+    // kernel waits for that kernel before its first global access.
+    cudaLaunchAttribute pattr[1];
+    pattr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pattr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = pattr;
+    cfg.numAttrs = 1;
     void *args[3] = {&p, &tmap_k, &tmap_v};
     cudaError_t e = cudaLaunchKernelExC(&cfg, k.fn, args);
     if (e != cudaSuccess) return fail_cuda("launch attention kernel", e);
   }
   if (!v2) return PA_OK;
-  // Phase 2 has work only for sequences of more than fuse_limit partitions.
-  if (max_parts_of(c.max_seq_len, c.partition_size) <= p.fuse_limit) return PA_OK;
+  // With the combine fused, Phase 2 has work only for sequences of more than
+  // fuse_limit partitions (Phase 1 then also wrote the empty ones' zeros).
+  if (p.fuse_limit > 0 && max_parts_of(c.max_seq_len, c.partition_size) <= p.fuse_limit)
+    return PA_OK;
   if (opt.phase1_event) {
     cudaError_t e = cudaEventRecord(static_cast<cudaEvent_t>(opt.phase1_event), c.stream);
     if (e != cudaSuccess) return fail_cuda("cudaEventRecord(phase1_event)", e);
@@ -380,22 +391,58 @@ pa_status_t launch(const Call &c, bool v2, const pa_options_t &opt) {
   r.partition_size = c.partition_size;
   r.max_seq_len = c.max_seq_len;
   r.fuse_limit = p.fuse_limit;
-  // Warps per (sequence, head): enough that each warp's chain of dependent
-  // tmp_out loads stays short; then split columns over CTAs until the grid
-  // covers the GPU twice.
-  const long long pairs = (long long)c.num_seqs * c.num_heads;
-  const int wph = p.max_parts <= 16 ? 1 : p.max_parts <= 32 ? 2 : p.max_parts <= 64 ? 4 : 8;
-  const long long groups = 8 / wph;
-  const long long ctas = (pairs + groups - 1) / groups;
-  int dsplit = 1;
-  while (ctas * dsplit < 2LL * dev->sm_count && c.head_size / (dsplit * 2) >= 32) dsplit *= 2;
-  r.cols_per_cta = c.head_size / dsplit;
-  r.warps_per_head = wph;
-  const void *rfn = reduce_kernel(c.dtype);
-  if (pairs == 0) return PA_OK;
+  // Team size W (warps per task) and column split: the pair that minimises
+  // (tasks per resident team) x (1 + rounds of loads for the longest
+  // sequence), where a round is one batch of NB partitions per thread.
+  const long long prows = (long long)c.num_seqs * c.num_heads;
+  if (prows == 0) return PA_OK;
+  int occ = 0;
+  {
+    const void *probe = reduce_kernel(c.dtype, 1);
+    pa_status_t so = occupancy(probe, 256, 0, &occ);
+    if (so != PA_OK) return so;
+    if (occ < 1) return PA_ERR_UNSUPPORTED;
+  }
+  const long long resident_warps = (long long)occ * dev->sm_count * 8;
+  int best_w = 1, best_ds = 1, best_vpt = 1;
+  long long best_cost = -1;
+  for (int w = 1; w <= 8; w *= 2) {
+    for (int ds = 1; c.head_size / 4 / ds >= 4; ds *= 2) {
+      const int f4 = c.head_size / 4 / ds;  // float4 columns per task
+      const int vpt = f4 > 32 ? f4 / 32 : 1;
+      if (vpt > 2) continue;
+      const int lanes = f4 / vpt;
+      const long long slots = (long long)w * (32 / lanes);
+      const long long nb = vpt == 1 ? 4 : 2;  // the kernel's batch (NB)
+      const long long rounds = (p.max_parts + slots * nb - 1) / (slots * nb);
+      const long long conc = resident_warps / w;
+      const long long waves = (prows * ds + conc - 1) / conc;
+      const long long cost = waves * (1 + rounds);
+      if (best_cost < 0 || cost < best_cost) {
+        best_cost = cost;
+        best_w = w;
+        best_ds = ds;
+        best_vpt = vpt;
+      }
+    }
+  }
+  r.cols_per_cta = c.head_size / best_ds;
+  r.warps_per_head = best_w;
+  const void *rfn = reduce_kernel(c.dtype, best_vpt);
+  if (!rfn) return PA_ERR_UNSUPPORTED;
+  int occ_k = 0;
+  {
+    pa_status_t so = occupancy(rfn, 256, 0, &occ_k);
+    if (so != PA_OK) return so;
+    if (occ_k < 1) return PA_ERR_UNSUPPORTED;
+  }
+  // persistent: never more CTAs than are resident at once
+  const long long teams_per_cta = 8 / best_w;
+  long long ctas = (prows * best_ds + teams_per_cta - 1) / teams_per_cta;
+  if (ctas > (long long)occ_k * dev->sm_count) ctas = (long long)occ_k * dev->sm_count;
   cudaLaunchConfig_t cfg;
   memset(&cfg, 0, sizeof cfg);
-  cfg.gridDim = dim3((unsigned)ctas, (unsigned)dsplit, 1);
+  cfg.gridDim = dim3((unsigned)ctas, 1, 1);
   cfg.blockDim = dim3(256, 1, 1);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = c.stream;

@@ -524,6 +524,11 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) __maxnreg__((kernel_max_regs
     fence_mbar_init();
   }
   __syncthreads();
+  // Launched with programmatic dependent launch: everything above touched
+  // only shared memory; wait here until the previous kernel in the stream has
+  // finished and its writes are visible (it may have produced the queries or
+  // the cache, or still be reading what this kernel writes).
+  pdl_wait_primary();
 
   const StageGeom geom{p.log2_unit_rows, p.unit_rows - 1, (uint32_t)p.unit_rows * kPanelBytes,
                        (uint32_t)(NPANELS * p.unit_rows * kPanelBytes)};
@@ -538,21 +543,61 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) __maxnreg__((kernel_max_regs
     }
     const int U = p.unit_rows;
     const int units_per_stage = ST / U;
-    // The first item of a CTA is its own index; later ones come from the
-    // counter, offset by the grid.  Lane 0 issues the atomic one item ahead
-    // and the value is broadcast only when that item is located.
-    auto grab_issue = [&]() -> int { return lane == 0 ? atomicAdd(p.sched, 1) : 0; };
-    auto grab_value = [&](int raw) -> int {
-      return (int)gridDim.x + __shfl_sync(0xffffffffu, raw, 0);
-    };
+    // Every K/V byte is read once: let those lines leave L2 first.
+    const uint64_t kv_policy = l2_policy_evict_first();
     // V2 locates an item through the running count of items per sequence;
     // the cursor (a chunk of 32 sequences, scanned once) only moves forward
     // because every CTA takes items in increasing order.
     int cs = 0, cbase = 0, c_cnt = 0, c_incl = 0, c_L = 0, c_total = 0;
     bool c_loaded = false;
+    auto load_chunk = [&]() {
+      const int sl = cs + lane;
+      c_L = 0;
+      if (sl < p.num_seqs) {
+        c_L = __ldg(p.seq_lens + sl);
+        if (c_L < 0 || c_L > p.max_seq_len) {
+          report(p.status, kStatusBadInput);
+          c_L = c_L < 0 ? 0 : p.max_seq_len;
+        }
+      }
+      // With the cross-partition combine fused into this kernel, an empty
+      // sequence gets one item per KV head that writes zeros; lanes past the
+      // last sequence count none.
+      const int c_np = (c_L + p.range_tokens - 1) / p.range_tokens;
+      c_cnt = sl >= p.num_seqs ? 0
+                               : p.num_kv_heads * (c_np == 0 && p.fuse_limit > 0 ? 1 : c_np);
+      c_incl = c_cnt;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, c_incl, off);
+        if (lane >= off) c_incl += t;
+      }
+      c_total = __shfl_sync(0xffffffffu, c_incl, 31);
+      c_loaded = true;
+    };
+    // The first item of a CTA is its own index; later ones come from the
+    // counter, offset by the number of CTAs that take items.  Lane 0 issues
+    // the atomic one item ahead and the value is broadcast only when that
+    // item is located.
+    int takers = (int)gridDim.x;
+    int item = blockIdx.x;
+    if (p.write_partials && p.num_seqs <= 32) {
+      // A batch of at most 32 sequences is counted in one chunk, so every CTA
+      // knows the number of items N.  When N is not a multiple of the grid
+      // (say 1.7 items per CTA) the CTAs that take one more item than the
+      // rest set the pace; so only ceil(N / ceil(N / grid)) CTAs take items,
+      // each the same number, and the others leave at once.
+      load_chunk();
+      const int per = (c_total + (int)gridDim.x - 1) / (int)gridDim.x;
+      takers = per > 0 ? (c_total + per - 1) / per : 0;
+      if ((int)blockIdx.x >= takers) item = c_total;  // past the last item: none
+    }
+    auto grab_issue = [&]() -> int { return lane == 0 ? atomicAdd(p.sched, 1) : 0; };
+    auto grab_value = [&](int raw) -> int {
+      return takers + __shfl_sync(0xffffffffu, raw, 0);
+    };
     int i = 0;  // stages issued by this CTA
     bool ok = true;
-    int item = blockIdx.x;
     while (true) {
       // ---- locate the item: (s, kvh, part, L)
       int s = 0, kvh = 0, part = 0, L = 0, np_s = 1;
@@ -572,32 +617,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) __maxnreg__((kernel_max_regs
         }
       } else {
         while (true) {
-          if (!c_loaded) {
-            const int sl = cs + lane;
-            c_L = 0;
-            if (sl < p.num_seqs) {
-              c_L = __ldg(p.seq_lens + sl);
-              if (c_L < 0 || c_L > p.max_seq_len) {
-                report(p.status, kStatusBadInput);
-                c_L = c_L < 0 ? 0 : p.max_seq_len;
-              }
-            }
-            // With the cross-partition combine fused into this kernel, an
-            // empty sequence gets one item per KV head that writes zeros;
-            // lanes past the last sequence count none.
-            const int c_np = (c_L + p.range_tokens - 1) / p.range_tokens;
-            c_cnt = sl >= p.num_seqs
-                        ? 0
-                        : p.num_kv_heads * (c_np == 0 && p.fuse_limit > 0 ? 1 : c_np);
-            c_incl = c_cnt;
-#pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-              const int t = __shfl_up_sync(0xffffffffu, c_incl, off);
-              if (lane >= off) c_incl += t;
-            }
-            c_total = __shfl_sync(0xffffffffu, c_incl, 31);
-            c_loaded = true;
-          }
+          if (!c_loaded) load_chunk();
           if (item < cbase + c_total) {
             const unsigned hit = __ballot_sync(0xffffffffu, cbase + c_incl > item);
             const int ls = __ffs(hit) - 1;
@@ -682,8 +702,10 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) __maxnreg__((kernel_max_regs
           const uint32_t vdst = kdst + HALF_BYTES;
 #pragma unroll
           for (int pn = 0; pn < NPANELS; ++pn) {
-            tma_load_2d(kdst + pn * geom.panel_bytes, &tmap_k, pn * (kPanelBytes / ELT), y, full0 + 8 * st);
-            tma_load_2d(vdst + pn * geom.panel_bytes, &tmap_v, pn * (kPanelBytes / ELT), y, full0 + 8 * st);
+            tma_load_2d_hint(kdst + pn * geom.panel_bytes, &tmap_k, pn * (kPanelBytes / ELT), y,
+                             full0 + 8 * st, kv_policy);
+            tma_load_2d_hint(vdst + pn * geom.panel_bytes, &tmap_v, pn * (kPanelBytes / ELT), y,
+                             full0 + 8 * st, kv_policy);
           }
         }
         if (first && lane == 0) {
@@ -907,6 +929,9 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) __maxnreg__((kernel_max_regs
       report(p.status, kStatusTimeout);
       flags[0] = 1;
     }
+    // Let the next kernel (Phase 2) be scheduled once every CTA is here; its
+    // own wait holds it until this grid has completed.  (Triggered earlier,
+    // its CTAs would crowd onto the few SMs that have room.)
     pdl_launch_dependents();
   }
 

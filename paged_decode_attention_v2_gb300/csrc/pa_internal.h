@@ -50,8 +50,8 @@ struct ReduceParams {
   int num_seqs, num_heads, head_size, max_parts, partition_size, max_seq_len;
   int fuse_limit;      // sequences of at most this many partitions were
                        // finished by Phase 1 (0 = none)
-  int cols_per_cta;    // head_size / gridDim.y
-  int warps_per_head;  // 1, 2, 4 or 8 warps share one (sequence, head)
+  int cols_per_cta;    // columns of one task: head_size / (column split)
+  int warps_per_head;  // warps of the team that serves one task: 1, 2, 4 or 8
 };
 
 enum MathKind { kMathSimt = 1, kMathTensor = 2 };
@@ -94,6 +94,6 @@ AttnKernelInfo attn_kernel_tensor_f16(int head_size, int group);
 AttnKernelInfo attn_kernel_simt_f32(int head_size, int group);
 AttnKernelInfo attn_kernel_simt_bf16(int head_size, int group);
 AttnKernelInfo attn_kernel_simt_f16(int head_size, int group);
-const void *reduce_kernel(int dtype);
+const void *reduce_kernel(int dtype, int float4_per_thread);
 
 }  // namespace pa

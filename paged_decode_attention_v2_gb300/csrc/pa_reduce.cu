@@ -5,15 +5,18 @@
 //   r_p   = exp(max_logits[p] - M) * exp_sums[p]
 //   out   = sum_p (r_p / sum_p' r_p') * tmp_out[p]
 //
-// A group of `wph` warps (1, 2, 4 or 8) serves one (sequence, query head) and
-// a slice of `cols_per_cta` columns of it; a 256-thread CTA holds 8 / wph such
-// groups.  Lanes form row groups of `lpr` lanes (one 16-byte column chunk
-// each); every row group walks its share of the partitions in one pass,
-// four at a time with all loads issued up front, keeping an online
-// log-sum-exp state: running max m, running sum S = sum r_p exp(-m) and the
-// running weighted row sum.  Row groups, then warps (through shared memory),
-// merge their states with the same rescale rule, so the result is the
-// formula above up to rounding.
+// A task is one (sequence, query head) and a slice of its columns.  A team
+// of W warps (1, 2, 4 or 8) serves one task at a time; a 256-thread CTA holds
+// 8 / W teams, and the grid is no larger than what is resident on the GPU at
+// once, so teams loop over tasks (persistent).  Inside a team, C lanes cover
+// the slice's float4 columns of one partition and the team's 32 * W / C
+// "slots" take the partitions slot, slot + S, ... (S slots); each thread
+// issues the loads of up to NB of its partitions at once and folds them into
+// an online log-sum-exp state: running max m, running sum S = sum r_p e^-m
+// and the running weighted row.  The slots' states are merged with the same
+// rescale rule (shuffles inside a warp, shared memory across the team), so
+// the result is the formula above up to rounding.  The host sizes W and the
+// column split so that one batch covers the longest sequence's partitions.
 #include <math_constants.h>
 
 #include "pa_device.cuh"
@@ -22,176 +25,192 @@ namespace pa {
 
 constexpr int kReduceThreads = 256;
 
-// Online LSE state of one lane: max, normaliser and up to 8 columns.
+// Online LSE state of one thread: max, normaliser and VPT float4 columns.
+template <int VPT>
 struct LseAcc {
   float m, S;
-  float4 a[2];
+  float4 a[VPT];
 };
 
-__device__ __forceinline__ void lse_merge(LseAcc &x, float m2, float S2, const float4 (&a2)[2],
-                                          int per_lane) {
+template <int VPT>
+__device__ __forceinline__ void lse_merge(LseAcc<VPT> &x, float m2, float S2,
+                                          const float4 (&a2)[VPT]) {
   const float M = fmaxf(x.m, m2);
   const float f1 = M == -CUDART_INF_F ? 0.f : expf(x.m - M);
   const float f2 = M == -CUDART_INF_F ? 0.f : expf(m2 - M);
   x.S = x.S * f1 + S2 * f2;
 #pragma unroll
-  for (int k = 0; k < 2; ++k)
-    if (k < per_lane) {
-      x.a[k].x = x.a[k].x * f1 + a2[k].x * f2;
-      x.a[k].y = x.a[k].y * f1 + a2[k].y * f2;
-      x.a[k].z = x.a[k].z * f1 + a2[k].z * f2;
-      x.a[k].w = x.a[k].w * f1 + a2[k].w * f2;
-    }
+  for (int k = 0; k < VPT; ++k) {
+    x.a[k].x = x.a[k].x * f1 + a2[k].x * f2;
+    x.a[k].y = x.a[k].y * f1 + a2[k].y * f2;
+    x.a[k].z = x.a[k].z * f1 + a2[k].z * f2;
+    x.a[k].w = x.a[k].w * f1 + a2[k].w * f2;
+  }
   x.m = M;
 }
 
-template <typename OutT>
-__global__ void __launch_bounds__(kReduceThreads)
-    pa_v2_reduce_kernel(const __grid_constant__ ReduceParams p) {
-  // With programmatic dependent launch this kernel may start before Phase 1
-  // has finished; wait here until all of its results are visible.
-  pdl_wait_primary();
-
-  __shared__ float4 part_a[kReduceThreads / 32][64];  // [warp][<= 256 cols / 4]
-  __shared__ float part_m[kReduceThreads / 32], part_S[kReduceThreads / 32];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int wph = p.warps_per_head;
-  const int groups = (kReduceThreads / 32) / wph;
-  const int g = warp / wph, wig = warp % wph;  // group in CTA, warp in group
-  const long long pair = (long long)blockIdx.x * groups + g;
-  const bool live = pair < (long long)p.num_seqs * p.num_heads;
-  const int s = live ? (int)(pair / p.num_heads) : 0;
-  const int h = live ? (int)(pair % p.num_heads) : 0;
-  const int D = p.head_size;
-  const int ncols = p.cols_per_cta;
-  const int col0 = blockIdx.y * ncols;
-
-  int np = 0;
-  bool done = !live;  // sequences that Phase 1 finished are left alone
-  if (live) {
-    int L = p.seq_lens[s];
-    L = L < 0 ? 0 : (L > p.max_seq_len ? p.max_seq_len : L);  // Phase 1 reported it
-    np = (L + p.partition_size - 1) / p.partition_size;
-    // With the combine fused (fuse_limit > 0) Phase 1 also wrote the zeros
-    // of empty sequences; without it, this kernel writes them.
-    if (p.fuse_limit > 0 && np <= p.fuse_limit) {
-      done = true;
-      np = 0;
-    }
-  }
-  const size_t row0 = ((size_t)s * p.num_heads + h) * p.max_parts;
-  const float *ml = p.max_logits + row0;
-  const float *es = p.exp_sums + row0;
-
-  const int c4 = ncols / 4;           // float4s per row
-  const int lpr = c4 < 32 ? c4 : 32;  // lanes per row
-  const int rpi = 32 / lpr;           // rows per warp iteration
-  const int per_lane = c4 / lpr;      // float4s per lane (1 or 2)
-  const int sub = lane / lpr, cl = lane % lpr;
-  const float *tmp = p.tmp_out + row0 * D + col0 + 4 * cl;
-  const int stride = wph * rpi;
-
-  LseAcc acc;
-  acc.m = -CUDART_INF_F;
-  acc.S = 0.f;
-  acc.a[0] = acc.a[1] = make_float4(0.f, 0.f, 0.f, 0.f);
-  int i = wig * rpi + sub;
-  for (; i < np; i += 4 * stride) {
-    float lm[4], le[4];
-    float4 v[4][2];
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int r = i + u * stride;
-      const bool ok = r < np;
-      lm[u] = ok ? __ldcg(ml + r) : -CUDART_INF_F;
-      le[u] = ok ? __ldcg(es + r) : 0.f;
-#pragma unroll
-      for (int k = 0; k < 2; ++k)
-        v[u][k] = (ok && k < per_lane)
-                      ? __ldcg(reinterpret_cast<const float4 *>(tmp + (size_t)r * D + 4 * lpr * k))
-                      : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-    float M = acc.m;
-#pragma unroll
-    for (int u = 0; u < 4; ++u) M = fmaxf(M, lm[u]);
-    const float f = acc.m == -CUDART_INF_F ? 0.f : expf(acc.m - M);
-    acc.S *= f;
-#pragma unroll
-    for (int k = 0; k < 2; ++k) {
-      acc.a[k].x *= f;
-      acc.a[k].y *= f;
-      acc.a[k].z *= f;
-      acc.a[k].w *= f;
-    }
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const float w = lm[u] == -CUDART_INF_F ? 0.f : expf(lm[u] - M) * le[u];
-      acc.S += w;
-#pragma unroll
-      for (int k = 0; k < 2; ++k) {
-        acc.a[k].x = fmaf(w, v[u][k].x, acc.a[k].x);
-        acc.a[k].y = fmaf(w, v[u][k].y, acc.a[k].y);
-        acc.a[k].z = fmaf(w, v[u][k].z, acc.a[k].z);
-        acc.a[k].w = fmaf(w, v[u][k].w, acc.a[k].w);
-      }
-    }
-    acc.m = M;
-  }
-  // merge the row groups of the warp (lanes with the same column chunk)
-  for (int off = lpr; off < 32; off <<= 1) {
-    const float m2 = __shfl_xor_sync(0xffffffffu, acc.m, off);
-    const float S2 = __shfl_xor_sync(0xffffffffu, acc.S, off);
-    float4 a2[2];
-#pragma unroll
-    for (int k = 0; k < 2; ++k) {
-      a2[k].x = __shfl_xor_sync(0xffffffffu, acc.a[k].x, off);
-      a2[k].y = __shfl_xor_sync(0xffffffffu, acc.a[k].y, off);
-      a2[k].z = __shfl_xor_sync(0xffffffffu, acc.a[k].z, off);
-      a2[k].w = __shfl_xor_sync(0xffffffffu, acc.a[k].w, off);
-    }
-    lse_merge(acc, m2, S2, a2, 2);
-  }
-  // merge the warps of the group
-  if (wph > 1) {
-    if (sub == 0) {
-#pragma unroll
-      for (int k = 0; k < 2; ++k)
-        if (k < per_lane) part_a[warp][cl + lpr * k] = acc.a[k];
-      if (lane == 0) {
-        part_m[warp] = acc.m;
-        part_S[warp] = acc.S;
-      }
-    }
-    __syncthreads();
-    if (wig != 0) return;
-    if (sub == 0)
-      for (int w2 = 1; w2 < wph; ++w2) {
-        float4 a2[2];
-#pragma unroll
-        for (int k = 0; k < 2; ++k)
-          a2[k] = k < per_lane ? part_a[warp + w2][cl + lpr * k] : make_float4(0.f, 0.f, 0.f, 0.f);
-        lse_merge(acc, part_m[warp + w2], part_S[warp + w2], a2, per_lane);
-      }
-  }
-  if (done || sub != 0) return;
-  OutT *out = static_cast<OutT *>(p.out) + ((size_t)s * p.num_heads + h) * D + col0;
-  const float inv = np > 0 ? 1.f / acc.S : 0.f;  // np == 0: empty sequence -> zeros
-#pragma unroll
-  for (int k = 0; k < 2; ++k)
-    if (k < per_lane) {
-      OutT *o = out + 4 * (cl + lpr * k);
-      o[0] = from_float<OutT>(acc.a[k].x * inv);
-      o[1] = from_float<OutT>(acc.a[k].y * inv);
-      o[2] = from_float<OutT>(acc.a[k].z * inv);
-      o[3] = from_float<OutT>(acc.a[k].w * inv);
-    }
+// Barrier of the W warps of team g (named barrier 1 + g; 0 is __syncthreads).
+__device__ __forceinline__ void team_sync(int g, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(1 + g), "r"(nthreads) : "memory");
 }
 
-const void *reduce_kernel(int dtype) {
-  switch (dtype) {
-    case 0: return reinterpret_cast<const void *>(&pa_v2_reduce_kernel<float>);
-    case 1: return reinterpret_cast<const void *>(&pa_v2_reduce_kernel<__nv_bfloat16>);
-    case 2: return reinterpret_cast<const void *>(&pa_v2_reduce_kernel<__half>);
+__device__ __forceinline__ int partitions_of(const ReduceParams &p, long long row) {
+  int L = __ldg(p.seq_lens + row / p.num_heads);
+  L = L < 0 ? 0 : (L > p.max_seq_len ? p.max_seq_len : L);  // Phase 1 reported it
+  return (L + p.partition_size - 1) / p.partition_size;
+}
+
+template <typename OutT, int VPT>
+__global__ void __launch_bounds__(kReduceThreads, 4)
+    pa_v2_reduce_kernel(const __grid_constant__ ReduceParams p) {
+  constexpr int NB = VPT == 1 ? 4 : 2;  // partitions per thread per batch of loads (no spills at 64 registers)
+  __shared__ float4 part_a[kReduceThreads / 32][32 * VPT];  // [warp][slice float4s]
+  __shared__ float part_m[kReduceThreads / 32], part_S[kReduceThreads / 32];
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int W = p.warps_per_head;
+  const int teams = (kReduceThreads / 32) / W;
+  const int g = warp / W, wig = warp % W;  // team in CTA, warp in team
+  const int D = p.head_size;
+  const int ncols = p.cols_per_cta;
+  const int C = ncols / (4 * VPT);  // lanes per partition row (<= 32)
+  const int spw = 32 / C;           // partition slots per warp
+  const int slot = wig * spw + lane / C, cl = lane % C;
+  const int S = W * spw;            // partitions advance by S per round
+  const int dsplit = D / ncols;
+  const long long ntasks = (long long)p.num_seqs * p.num_heads * dsplit;
+  const long long tstride = (long long)gridDim.x * teams;
+  long long task = (long long)blockIdx.x * teams + g;
+
+  // seq_lens is an input, not a Phase 1 result: read the first task's before
+  // waiting for Phase 1 (programmatic dependent launch), later ones a task
+  // ahead.
+  int np_next = task < ntasks ? partitions_of(p, task / dsplit) : 0;
+  pdl_wait_primary();
+  pdl_launch_dependents();  // the next kernel still waits for this grid to complete
+
+  for (; task < ntasks; task += tstride) {
+    const long long row = task / dsplit;  // s * num_heads + h
+    const int col0 = (int)(task % dsplit) * ncols;
+    int np = np_next;
+    if (task + tstride < ntasks) np_next = partitions_of(p, (task + tstride) / dsplit);
+    // With the combine fused into Phase 1 (fuse_limit > 0) it finished these
+    // sequences, empty ones included; without it, this kernel writes the
+    // zeros of empty sequences.
+    const bool done = p.fuse_limit > 0 && np <= p.fuse_limit;
+    if (done) np = 0;
+
+    const float *ml = p.max_logits + row * p.max_parts;
+    const float *es = p.exp_sums + row * p.max_parts;
+    const float *tmp = p.tmp_out + row * p.max_parts * D + col0 + 4 * cl;
+
+    LseAcc<VPT> acc;
+    acc.m = -CUDART_INF_F;
+    acc.S = 0.f;
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) acc.a[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int i = slot; i < np; i += NB * S) {
+      float lm[NB], le[NB];
+      float4 v[NB][VPT];
+#pragma unroll
+      for (int u = 0; u < NB; ++u) {
+        const int r = i + u * S;
+        const bool ok = r < np;
+        lm[u] = ok ? __ldcg(ml + r) : -CUDART_INF_F;
+        le[u] = ok ? __ldcg(es + r) : 0.f;
+#pragma unroll
+        for (int k = 0; k < VPT; ++k)
+          v[u][k] = ok ? __ldcg(reinterpret_cast<const float4 *>(tmp + (size_t)r * D + 4 * C * k))
+                       : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+      float M = acc.m;
+#pragma unroll
+      for (int u = 0; u < NB; ++u) M = fmaxf(M, lm[u]);
+      const float f = acc.m == -CUDART_INF_F ? 0.f : expf(acc.m - M);
+      acc.S *= f;
+#pragma unroll
+      for (int k = 0; k < VPT; ++k) {
+        acc.a[k].x *= f;
+        acc.a[k].y *= f;
+        acc.a[k].z *= f;
+        acc.a[k].w *= f;
+      }
+#pragma unroll
+      for (int u = 0; u < NB; ++u) {
+        const float w = lm[u] == -CUDART_INF_F ? 0.f : expf(lm[u] - M) * le[u];
+        acc.S += w;
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) {
+          acc.a[k].x = fmaf(w, v[u][k].x, acc.a[k].x);
+          acc.a[k].y = fmaf(w, v[u][k].y, acc.a[k].y);
+          acc.a[k].z = fmaf(w, v[u][k].z, acc.a[k].z);
+          acc.a[k].w = fmaf(w, v[u][k].w, acc.a[k].w);
+        }
+      }
+      acc.m = M;
+    }
+    // merge the slots of the warp (lanes with the same column chunk)
+    for (int off = C; off < 32; off <<= 1) {
+      const float m2 = __shfl_xor_sync(0xffffffffu, acc.m, off);
+      const float S2 = __shfl_xor_sync(0xffffffffu, acc.S, off);
+      float4 a2[VPT];
+#pragma unroll
+      for (int k = 0; k < VPT; ++k) {
+        a2[k].x = __shfl_xor_sync(0xffffffffu, acc.a[k].x, off);
+        a2[k].y = __shfl_xor_sync(0xffffffffu, acc.a[k].y, off);
+        a2[k].z = __shfl_xor_sync(0xffffffffu, acc.a[k].z, off);
+        a2[k].w = __shfl_xor_sync(0xffffffffu, acc.a[k].w, off);
+      }
+      lse_merge(acc, m2, S2, a2);
+    }
+    // merge the warps of the team through shared memory
+    if (W > 1) {
+      if (lane < C) {
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) part_a[warp][cl + C * k] = acc.a[k];
+        if (lane == 0) {
+          part_m[warp] = acc.m;
+          part_S[warp] = acc.S;
+        }
+      }
+      team_sync(g, W * 32);
+      if (wig == 0 && lane < C)
+        for (int w2 = 1; w2 < W; ++w2) {
+          float4 a2[VPT];
+#pragma unroll
+          for (int k = 0; k < VPT; ++k) a2[k] = part_a[warp + w2][cl + C * k];
+          lse_merge(acc, part_m[warp + w2], part_S[warp + w2], a2);
+        }
+    }
+    if (!done && wig == 0 && lane < C) {
+      OutT *out = static_cast<OutT *>(p.out) + row * D + col0;
+      const float inv = np > 0 ? 1.f / acc.S : 0.f;  // np == 0: empty sequence -> zeros
+#pragma unroll
+      for (int k = 0; k < VPT; ++k) {
+        OutT *o = out + 4 * (cl + C * k);
+        o[0] = from_float<OutT>(acc.a[k].x * inv);
+        o[1] = from_float<OutT>(acc.a[k].y * inv);
+        o[2] = from_float<OutT>(acc.a[k].z * inv);
+        o[3] = from_float<OutT>(acc.a[k].w * inv);
+      }
+    }
+    if (W > 1) team_sync(g, W * 32);  // the shared slots are free for the next task
+  }
+}
+
+const void *reduce_kernel(int dtype, int vpt) {
+  if (vpt == 1) {
+    switch (dtype) {
+      case 0: return reinterpret_cast<const void *>(&pa_v2_reduce_kernel<float, 1>);
+      case 1: return reinterpret_cast<const void *>(&pa_v2_reduce_kernel<__nv_bfloat16, 1>);
+      case 2: return reinterpret_cast<const void *>(&pa_v2_reduce_kernel<__half, 1>);
+    }
+  } else if (vpt == 2) {
+    switch (dtype) {
+      case 0: return reinterpret_cast<const void *>(&pa_v2_reduce_kernel<float, 2>);
+      case 1: return reinterpret_cast<const void *>(&pa_v2_reduce_kernel<__nv_bfloat16, 2>);
+      case 2: return reinterpret_cast<const void *>(&pa_v2_reduce_kernel<__half, 2>);
+    }
   }
   return nullptr;
 }

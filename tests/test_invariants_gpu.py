@@ -116,16 +116,17 @@ def test_fused_combine_reads_every_partition():
     through the fused combine repeatedly and must match the oracle to 1e-5."""
     warm = workloads.make_case("warm", 7, 3, 16, 2, 128, torch.bfloat16, 16, [1, 700, 1300],
                                partition_size=512, extra_blocks=4)
-    DeviceCase(warm).run(variant=pa.PA_VARIANT_V2)
+    DeviceCase(warm).run(variant=pa.PA_VARIANT_V2, fuse_partitions=16)
     case = workloads.make_case("fused", 8, 2, 4, 1, 64, torch.float32, 16, [37, 1000],
                                partition_size=256, extra_blocks=2)
     ref = reference(case)
     dc = DeviceCase(case)
     for _ in range(8):
-        assert_close(dc.run(variant=pa.PA_VARIANT_V2), ref, torch.float32, "fused combine")
+        assert_close(dc.run(variant=pa.PA_VARIANT_V2, fuse_partitions=16), ref, torch.float32,
+                     "fused combine")
 
 
-@pytest.mark.parametrize("fuse", [0, -1])
+@pytest.mark.parametrize("fuse", [16, 0])
 @pytest.mark.parametrize("dtype,H,Hkv,D", [(torch.float32, 4, 1, 64), (torch.bfloat16, 16, 2, 128)])
 def test_writes_stay_inside_out_and_workspace(dtype, H, Hkv, D, fuse):
     """Regression: every write lands inside `out` and the workspace.  Both are

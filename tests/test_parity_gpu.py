@@ -74,11 +74,11 @@ def test_small_ragged(dtype, D, G, bs):
             assert_close(out, ref, dtype, f"math {math} v{variant}")
 
 
-@pytest.mark.parametrize("fuse", [-1, 1, 4, 0])
+@pytest.mark.parametrize("fuse", [-1, 0, 1, 4, 16, 64])
 @pytest.mark.parametrize("name", ["c2_gqa_batch8", "c5_mixed_d256"])
 def test_fused_combine_limits(name, fuse):
     """The cross-partition combine inside Phase 1 for sequences of at most
-    `fuse` partitions (-1: never, 0: the default of 16): same result."""
+    min(`fuse`, 16) partitions (0, the default, and -1: never): same result."""
     dc = device_config(name, 512 if name == "c5_mixed_d256" else None)
     for _ in range(2):  # twice: the combine counters must be left at zero
         out = dc.run(variant=pa.PA_VARIANT_V2, fuse_partitions=fuse)
