@@ -392,8 +392,11 @@ pa_status_t launch(const Call &c, bool v2, const pa_options_t &opt) {
   r.max_seq_len = c.max_seq_len;
   r.fuse_limit = p.fuse_limit;
   // Team size W (warps per task) and column split: the pair that minimises
-  // (tasks per resident team) x (1 + rounds of loads for the longest
-  // sequence), where a round is one batch of NB partitions per thread.
+  // the chain of the longest task (1 + its rounds of loads, a round being one
+  // batch of NB partitions per thread) plus 2 for every further wave of
+  // tasks (the typical task, with sequences of mixed lengths, takes one
+  // round).  Only max_seq_len is known here, so the longest task is sized
+  // from it.
   const long long prows = (long long)c.num_seqs * c.num_heads;
   if (prows == 0) return PA_OK;
   int occ = 0;
@@ -417,7 +420,7 @@ pa_status_t launch(const Call &c, bool v2, const pa_options_t &opt) {
       const long long rounds = (p.max_parts + slots * nb - 1) / (slots * nb);
       const long long conc = resident_warps / w;
       const long long waves = (prows * ds + conc - 1) / conc;
-      const long long cost = waves * (1 + rounds);
+      const long long cost = (1 + rounds) + 2 * (waves - 1);
       if (best_cost < 0 || cost < best_cost) {
         best_cost = cost;
         best_w = w;
