@@ -85,7 +85,7 @@ def test_fused_combine_limits(name, fuse):
         assert_close(out, reference(dc.case), dc.case.dtype, f"fuse={fuse}")
 
 
-@pytest.mark.parametrize("P", [64, 128, 512, 1024])
+@pytest.mark.parametrize("P", [64, 128, 512, 1024, 2048, 8192])
 def test_partition_sizes(P):
     lens = [1, P - 1, P, P + 1, 5 * P + 3, 1000]
     case = workloads.make_case("psweep", 77 + P, len(lens), 8, 1, 128, torch.bfloat16, 16, lens,
@@ -190,3 +190,41 @@ def test_sampled_outputs_at_full_size_long_context():
                                  dc.case.block_tables, dc.case.seq_lens, dc.case.scale)
     for i, (s, h) in enumerate(pairs):
         assert_close(torch.from_numpy(out[s, h]), ref[i], torch.bfloat16, f"pair {(s, h)}")
+
+
+def test_shared_prefix_blocks():
+    """Block tables that share physical blocks, as prefix caching leaves them:
+    sequences 1-3 start with sequence 0's first 40 blocks (640 tokens), and
+    sequence 3 also repeats one block inside its own table."""
+    import dataclasses
+    lens = [2000, 1500, 900, 3000]
+    base = workloads.make_case("shared", 17, len(lens), 32, 4, 128, torch.bfloat16, 16, lens,
+                               partition_size=512, extra_blocks=4)
+    bt = base.block_tables.clone()
+    for s in (1, 2, 3):
+        bt[s, :40] = bt[0, :40]
+    bt[3, 100] = bt[3, 50]
+    case = dataclasses.replace(base, block_tables=bt)
+    ref = reference(case)
+    dc = DeviceCase(case)
+    for variant in (pa.PA_VARIANT_V1, pa.PA_VARIANT_V2):
+        assert_close(dc.run(variant=variant), ref, torch.bfloat16, f"v{variant}")
+
+
+def test_very_long_sequences_sampled():
+    """Two sequences of 300K tokens (586 partitions each) and a short one:
+    Phase 2 at its widest; checked on sampled (seq, head) pairs computed one
+    by one by the oracle."""
+    import oracle
+    lens = [300000, 299999, 77]
+    case = workloads.make_case("verylong", 23, len(lens), 16, 2, 128, torch.bfloat16, 16, lens,
+                               partition_size=512)
+    dc = DeviceCase(case)
+    pairs = [(0, 0), (0, 15), (1, 3), (1, 8), (2, 9)]
+    ref = oracle.attention_pairs(pairs, case.query, case.key_cache, case.value_cache,
+                                 case.block_tables, case.seq_lens, case.scale)
+    for variant in (pa.PA_VARIANT_V2, pa.PA_VARIANT_V1):
+        out = dc.run(variant=variant).double().cpu().numpy()
+        for i, (s_, h) in enumerate(pairs):
+            assert_close(torch.from_numpy(out[s_, h]), ref[i], torch.bfloat16,
+                         f"v{variant} pair {(s_, h)}")
