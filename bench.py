@@ -308,26 +308,28 @@ def time_steps(runner, steps, flush, with_phase=False):
 
 
 def time_e2e(runner, steps, flush):
-    """The same step through the public API from pinned HOST buffers: the
-    query, block table and lengths are copied in and the output copied out
-    inside the timed region."""
+    """The same step through the library's host-buffer C-ABI call
+    (pa_forward_host) from pinned HOST buffers: the query, block table and
+    lengths are copied in and the output copied out inside the timed region,
+    by the call itself."""
     c = runner.case
+    pa = runner.pa
     hq = c.query.pin_memory()
     hbt = c.block_tables.pin_memory()
     hsl = c.seq_lens.pin_memory()
     hout = torch.empty(c.query.shape, dtype=c.query.dtype).pin_memory()
-    dq, dbt, dsl = torch.empty_like(runner.q), torch.empty_like(runner.bt), \
-        torch.empty_like(runner.sl)
+    staging = pa.alloc_staging(hq, hbt, device=runner.device)
     E = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
     starts, ends = [E() for _ in range(steps)], [E() for _ in range(steps)]
     for i in range(steps):
         flush.zero_()
         starts[i].record()
-        dq.copy_(hq, non_blocking=True)
-        dbt.copy_(hbt, non_blocking=True)
-        dsl.copy_(hsl, non_blocking=True)
-        runner.step(q=dq, bt=dbt, sl=dsl, out=runner.out)
-        hout.copy_(runner.out, non_blocking=True)
+        pa.pa_forward_host(hout, hq, runner.kc, runner.vc, hbt, hsl, c.scale,
+                           c.partition_size, staging, runner.ws,
+                           max_seq_len=runner.max_seq_len, variant=runner.variant,
+                           math=runner.math, num_stages=runner.stages,
+                           ctas_per_sm=runner.ctas_per_sm,
+                           fuse_partitions=runner.fuse_partitions)
         ends[i].record()
     torch.cuda.synchronize()
     ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]

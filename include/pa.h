@@ -164,6 +164,41 @@ pa_status_t pa_forward(void *out, const void *query, const void *key_cache,
                        void *workspace, size_t workspace_bytes, void *stream,
                        const pa_options_t *opts);
 
+/* Device bytes of the staging buffer pa_forward_host needs: the query and
+ * the output ([num_seqs][num_heads][head_size] in the dtype), the block
+ * tables and seq_lens, each part 256-byte aligned.  Returns 0 on bad
+ * arguments. */
+size_t pa_host_staging_bytes(int num_seqs, int num_heads, int head_size,
+                             int max_blocks_per_seq, int dtype);
+
+/* pa_forward with the per-step data in HOST memory: query_host,
+ * block_tables_host and seq_lens_host are read from the host and out_host is
+ * written on the host (same layouts as pa_forward).  The KV caches and the
+ * workspace stay on the device.  `staging` is a caller-owned device buffer of
+ * at least pa_host_staging_bytes(...) bytes, 256-byte aligned.
+ *
+ * Enqueues on `stream`, in order: one host-to-device copy each of seq_lens,
+ * the block tables and the query into the staging buffer; the kernels of
+ * pa_forward; one device-to-host copy of the output.  It returns when they
+ * are enqueued: synchronise the stream before reading out_host.  Host
+ * buffers in pinned memory let the copies run asynchronously; pageable ones
+ * work too (the copies then synchronise the host with the stream).  The host
+ * buffers and the staging buffer must stay untouched until the stream
+ * reaches the end of the call.  Errors: as pa_forward, plus
+ * PA_ERR_INVALID_ARG for a null host pointer or a staging buffer that is
+ * null, misaligned or smaller than pa_host_staging_bytes(...). */
+pa_status_t pa_forward_host(void *out_host, const void *query_host,
+                            const void *key_cache, const void *value_cache,
+                            const int32_t *block_tables_host,
+                            const int32_t *seq_lens_host, int num_seqs,
+                            int num_heads, int num_kv_heads, int head_size,
+                            int num_blocks, int block_size,
+                            int max_blocks_per_seq, int max_seq_len,
+                            float scale, int partition_size, int dtype,
+                            void *staging, size_t staging_bytes,
+                            void *workspace, size_t workspace_bytes,
+                            void *stream, const pa_options_t *opts);
+
 /* V2 for callers that cannot allocate device memory, for example a plug-in
  * whose host framework owns all device memory and forbids cudaMalloc while
  * it serves a request, or a serving loop that must not pay cudaMalloc's

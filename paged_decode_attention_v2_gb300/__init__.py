@@ -42,7 +42,7 @@ _DTYPES = {torch.float32: PA_DTYPE_F32, torch.bfloat16: PA_DTYPE_BF16,
 EXPORTS = ("pa_workspace_bytes", "pa_workspace_layout", "pa_workspace_init",
            "pa_v1_forward", "pa_v2_forward", "pa_forward", "pa_choose_v2",
            "pa_read_device_status", "pa_status_string", "pa_last_cuda_error",
-           "pa_version", "pa_v2_forward_noalloc")
+           "pa_version", "pa_v2_forward_noalloc", "pa_host_staging_bytes", "pa_forward_host")
 
 
 class PAError(RuntimeError):
@@ -92,6 +92,11 @@ def load_library(path: str = LIB_PATH):
         lib.pa_v2_forward_noalloc.argtypes = _FWD_ARGS[:17] + [vp]
         lib.pa_forward.restype = ci
         lib.pa_forward.argtypes = _FWD_ARGS + [ctypes.POINTER(pa_options_t)]
+        lib.pa_host_staging_bytes.restype = cs
+        lib.pa_host_staging_bytes.argtypes = [ci] * 5
+        lib.pa_forward_host.restype = ci
+        lib.pa_forward_host.argtypes = (_FWD_ARGS[:17] + [vp, cs] + _FWD_ARGS[17:] +
+                                        [ctypes.POINTER(pa_options_t)])
         lib.pa_choose_v2.restype = ci
         lib.pa_choose_v2.argtypes = [ci] * 5
         lib.pa_read_device_status.restype = ci
@@ -227,6 +232,41 @@ def pa_forward(out, query, key_cache, value_cache, block_tables, seq_lens, scale
     _check(load_library().pa_forward(*_fwd_args(
         out, query, key_cache, value_cache, block_tables, seq_lens, scale, partition_size,
         workspace, max_seq_len, stream), ctypes.byref(opts)), "pa_forward")
+
+
+def pa_host_staging_bytes(num_seqs: int, num_heads: int, head_size: int,
+                          max_blocks_per_seq: int, dtype) -> int:
+    """Device bytes pa_forward_host stages the per-step data in."""
+    code = _DTYPES[dtype] if isinstance(dtype, torch.dtype) else int(dtype)
+    return int(load_library().pa_host_staging_bytes(num_seqs, num_heads, head_size,
+                                                    max_blocks_per_seq, code))
+
+
+def alloc_staging(query, block_tables, device=None) -> torch.Tensor:
+    """A device staging buffer for pa_forward_host calls of this shape."""
+    B, H, D = query.shape
+    n = pa_host_staging_bytes(B, H, D, block_tables.shape[1], query.dtype)
+    return torch.empty(max(n, 256), dtype=torch.uint8, device=device or "cuda")
+
+
+def pa_forward_host(out_host, query_host, key_cache, value_cache, block_tables_host,
+                    seq_lens_host, scale, partition_size, staging, workspace, max_seq_len=None,
+                    stream=None, variant=PA_VARIANT_AUTO, math=PA_MATH_AUTO, num_stages=0,
+                    ctas_per_sm=0, fuse_partitions=0) -> None:
+    """pa_forward with the query, block tables, lengths and output in host
+    memory (pinned for asynchronous copies): one C-ABI call enqueues the
+    host-to-device copies into ``staging``, the kernels and the copy of the
+    output back to ``out_host``.  Synchronise the stream before reading it."""
+    for t in (out_host, query_host, block_tables_host, seq_lens_host):
+        if t.is_cuda or not t.is_contiguous():
+            raise ValueError("pa_forward_host takes contiguous host tensors for "
+                             "out, query, block_tables and seq_lens")
+    opts = pa_options_t(variant, math, num_stages, 0, 0, None, ctas_per_sm, fuse_partitions)
+    args = _fwd_args(out_host, query_host, key_cache, value_cache, block_tables_host,
+                     seq_lens_host, scale, partition_size, workspace, max_seq_len, stream)
+    _check(load_library().pa_forward_host(
+        *args[:17], _ptr(staging), staging.numel() * staging.element_size(), *args[17:],
+        ctypes.byref(opts)), "pa_forward_host")
 
 
 def pa_choose_v2(num_seqs: int, num_kv_heads: int, max_seq_len: int, partition_size: int,

@@ -472,25 +472,32 @@ Call make_call(void *out, const void *query, const void *key_cache, const void *
               static_cast<cudaStream_t>(stream)};
 }
 
-pa_status_t run(const Call &c, int variant, const pa_options_t &opt) {
-  bool v2;
+// The variant a call runs (V1 or V2) and the full argument check for it;
+// nothing is enqueued.
+pa_status_t resolve(const Call &c, int variant, bool *v2) {
   if (variant == PA_VARIANT_V1) {
-    v2 = false;
+    *v2 = false;
   } else if (variant == PA_VARIANT_V2) {
-    v2 = true;
+    *v2 = true;
   } else if (variant == PA_VARIANT_AUTO) {
     pa_status_t st0 = check_args(c, false);
     if (st0 != PA_OK) return st0;
+    *v2 = false;
     if (c.num_seqs == 0) return PA_OK;
     DeviceFacts *dev = nullptr;
     pa_status_t st = device_facts(&dev);
     if (st != PA_OK) return st;
-    v2 = pa_choose_v2(c.num_seqs, c.num_kv_heads, c.max_seq_len, c.partition_size,
-                      dev->sm_count) != 0;
+    *v2 = pa_choose_v2(c.num_seqs, c.num_kv_heads, c.max_seq_len, c.partition_size,
+                       dev->sm_count) != 0;
   } else {
     return PA_ERR_INVALID_ARG;
   }
-  pa_status_t st = check_args(c, v2);
+  return check_args(c, *v2);
+}
+
+pa_status_t run(const Call &c, int variant, const pa_options_t &opt) {
+  bool v2 = false;
+  pa_status_t st = resolve(c, variant, &v2);
   if (st != PA_OK) return st;
   if (c.num_seqs == 0) return PA_OK;
   return launch(c, v2, opt);
@@ -578,6 +585,65 @@ pa_status_t pa_forward(void *out, const void *query, const void *key_cache,
                        max_blocks_per_seq, max_seq_len, scale, partition_size, dtype, workspace,
                        workspace_bytes, stream),
              opt.variant, opt);
+}
+
+size_t pa_host_staging_bytes(int num_seqs, int num_heads, int head_size,
+                             int max_blocks_per_seq, int dtype) {
+  if (num_seqs < 0 || num_heads < 1 || head_size < 1 || max_blocks_per_seq < 1 ||
+      (dtype != PA_DTYPE_F32 && dtype != PA_DTYPE_BF16 && dtype != PA_DTYPE_F16))
+    return 0;
+  const size_t qo = align256((size_t)num_seqs * num_heads * head_size * elt_size(dtype));
+  return 2 * qo + align256((size_t)num_seqs * max_blocks_per_seq * 4) +
+         align256((size_t)num_seqs * 4) + (num_seqs == 0 ? 256 : 0);
+}
+
+pa_status_t pa_forward_host(void *out_host, const void *query_host, const void *key_cache,
+                            const void *value_cache, const int32_t *block_tables_host,
+                            const int32_t *seq_lens_host, int num_seqs, int num_heads,
+                            int num_kv_heads, int head_size, int num_blocks, int block_size,
+                            int max_blocks_per_seq, int max_seq_len, float scale,
+                            int partition_size, int dtype, void *staging, size_t staging_bytes,
+                            void *workspace, size_t workspace_bytes, void *stream,
+                            const pa_options_t *opts) {
+  if (!out_host || !query_host || !block_tables_host || !seq_lens_host || !staging ||
+      !aligned(staging, 256))
+    return PA_ERR_INVALID_ARG;
+  const size_t need =
+      pa_host_staging_bytes(num_seqs, num_heads, head_size, max_blocks_per_seq, dtype);
+  if (need == 0 || staging_bytes < need) return PA_ERR_INVALID_ARG;
+  pa_options_t opt;
+  memset(&opt, 0, sizeof opt);
+  if (opts) opt = *opts;
+  // staging: query | out | block tables | seq_lens
+  const size_t qbytes = (size_t)num_seqs * num_heads * head_size * elt_size(dtype);
+  const size_t tbytes = (size_t)num_seqs * max_blocks_per_seq * 4;
+  uint8_t *st = static_cast<uint8_t *>(staging);
+  void *q_dev = st;
+  void *out_dev = st + align256(qbytes);
+  int32_t *bt_dev = reinterpret_cast<int32_t *>(st + 2 * align256(qbytes));
+  int32_t *sl_dev = reinterpret_cast<int32_t *>(st + 2 * align256(qbytes) + align256(tbytes));
+  const Call c = make_call(out_dev, q_dev, key_cache, value_cache, bt_dev, sl_dev, num_seqs,
+                           num_heads, num_kv_heads, head_size, num_blocks, block_size,
+                           max_blocks_per_seq, max_seq_len, scale, partition_size, dtype,
+                           workspace, workspace_bytes, stream);
+  // argument problems are reported before anything is enqueued
+  bool v2 = false;
+  pa_status_t chk = resolve(c, opt.variant, &v2);
+  if (chk != PA_OK) return chk;
+  if (num_seqs == 0) return PA_OK;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemcpyAsync(sl_dev, seq_lens_host, (size_t)num_seqs * 4,
+                                  cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) return fail_cuda("cudaMemcpyAsync(seq_lens)", e);
+  e = cudaMemcpyAsync(bt_dev, block_tables_host, tbytes, cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) return fail_cuda("cudaMemcpyAsync(block_tables)", e);
+  e = cudaMemcpyAsync(q_dev, query_host, qbytes, cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) return fail_cuda("cudaMemcpyAsync(query)", e);
+  pa_status_t r = launch(c, v2, opt);
+  if (r != PA_OK) return r;
+  e = cudaMemcpyAsync(out_host, out_dev, qbytes, cudaMemcpyDeviceToHost, s);
+  if (e != cudaSuccess) return fail_cuda("cudaMemcpyAsync(out)", e);
+  return PA_OK;
 }
 
 int pa_choose_v2(int num_seqs, int num_kv_heads, int max_seq_len, int partition_size,

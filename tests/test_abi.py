@@ -148,3 +148,12 @@ def test_workspace_init_rejects_bad_buffers(lib):
     assert lib.pa_workspace_init(0, 256, 0) == pa.PA_ERR_INVALID_ARG
     assert lib.pa_workspace_init(FAKE, 128, 0) == pa.PA_ERR_INVALID_ARG
     assert lib.pa_read_device_status(FAKE + 4, 0) == pa.PA_ERR_INVALID_ARG
+
+
+def test_host_staging_bytes(lib):
+    # query and out (B*H*D*elt each), block tables, seq_lens; 256-byte parts
+    assert pa.pa_host_staging_bytes(3, 8, 128, 10, pa.PA_DTYPE_BF16) == 6144 * 2 + 256 + 256
+    assert pa.pa_host_staging_bytes(3, 8, 128, 100, pa.PA_DTYPE_F32) == \
+        12288 * 2 + 1280 + 256
+    assert pa.pa_host_staging_bytes(-1, 8, 128, 10, pa.PA_DTYPE_BF16) == 0
+    assert pa.pa_host_staging_bytes(3, 8, 128, 10, 7) == 0
