@@ -90,6 +90,9 @@ def _declare(lib):
         ci, ci, dp]
     lib.pa_oracle_combine.restype = None
     lib.pa_oracle_combine.argtypes = [dp, dp, dp, dp, i32p, ci, ci, ci, ci]
+    lib.pa_oracle_query_chunks.restype = None
+    lib.pa_oracle_query_chunks.argtypes = [
+        dp, vp, vp, vp, ci, i32p, i32p, i32p, ci, ci, ci, ci, ci, ci, cd, ci, dp, ci]
     return lib
 
 
@@ -191,6 +194,35 @@ def attention_pairs(pairs, q, k_cache, v_cache, block_tables, seq_lens,
         ctypes.c_void_p(vc.data_ptr()), _dtype_code(q),
         ctypes.c_void_p(bt.data_ptr()), ctypes.c_void_p(sl.data_ptr()),
         B, H, Hkv, D, bs, mb, float(scale), nt, _dptr(scratch), maxL)
+    return out
+
+
+def query_chunks(q, k_cache, v_cache, block_tables, seq_lens, q_start, scale: float,
+                 nthreads: int = 0, lib=None) -> np.ndarray:
+    """Multi-token queries over the paged cache (the causal reading in
+    pa_oracle.c): q [rows, H, D], the chunk of sequence s being rows
+    q_start[s] .. q_start[s+1]-1, its last tokens.  Returns out [rows, H, D]."""
+    lib = lib or _get_lib()
+    q, kc, vc = (_cpu_contig(x) for x in (q, k_cache, v_cache))
+    if not (q.dtype == kc.dtype == vc.dtype):
+        raise ValueError("q, k_cache and v_cache must share one dtype")
+    bt = _cpu_contig(block_tables).to(torch.int32)
+    sl = _cpu_contig(seq_lens).to(torch.int32)
+    qs = _cpu_contig(torch.as_tensor(q_start)).to(torch.int32)
+    R, H, D = q.shape
+    nb, Hkv, bs, D2 = kc.shape
+    B = sl.numel()
+    if D2 != D or qs.numel() != B + 1 or int(qs[-1]) != R or H % Hkv:
+        raise ValueError("inconsistent shapes")
+    maxL = max(int(sl.max().item()) if B else 0, 1)
+    nt = nthreads if nthreads > 0 else lib.pa_oracle_max_threads()
+    scratch = np.empty(nt * maxL, dtype=np.float64)
+    out = np.zeros((R, H, D), dtype=np.float64)
+    lib.pa_oracle_query_chunks(
+        _dptr(out), ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(kc.data_ptr()),
+        ctypes.c_void_p(vc.data_ptr()), _dtype_code(q), ctypes.c_void_p(bt.data_ptr()),
+        ctypes.c_void_p(sl.data_ptr()), ctypes.c_void_p(qs.data_ptr()), B, H, Hkv, D, bs,
+        bt.shape[1], float(scale), nt, _dptr(scratch), maxL)
     return out
 
 

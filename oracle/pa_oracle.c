@@ -267,3 +267,70 @@ void pa_oracle_combine(double *out, const double *max_logits,
     }
   }
 }
+
+/* Multi-token queries over the paged cache: the query chunk of a sequence is
+ * its last few tokens, all of them already in the cache.  The prefill patch
+ * of project_6 (optimizations/prefix_prefill_patch.py, module docstring)
+ * tunes a kernel that runs attention for blocks of query positions over a
+ * paged prefix; the pages give no formula for it, so this is the plain
+ * causal reading:
+ *
+ *   sequence s holds L = seq_lens[s] tokens in the cache; its chunk is the
+ *   last n = q_start[s+1] - q_start[s] of them (1 <= n <= L), rows
+ *   q_start[s] .. q_start[s+1]-1 of q and out ([rows][H][D]);
+ *   chunk token i (cache position L - n + i) attends to cache tokens
+ *   [0, L - n + i]:
+ *     out[q_start[s] + i][h] = sum_{t <= L-n+i} softmax_t(scale q.K_t) V_t
+ *
+ * With n = 1 for every sequence this is pa_oracle_attention.  A sequence
+ * with n = 0 has no rows; n > L is not a valid input (its rows are left at
+ * zero).  Written out here on its own, not through attend_range, so that the
+ * two definitions can be checked against each other. */
+void pa_oracle_query_chunks(double *out, const void *q, const void *k_cache,
+                            const void *v_cache, int dtype,
+                            const int32_t *block_tables,
+                            const int32_t *seq_lens, const int32_t *q_start,
+                            int B, int H, int Hkv, int D, int bs,
+                            int max_blocks, double scale, int nthreads,
+                            double *logit_scratch, int max_seq_len) {
+  set_threads(nthreads);
+  const int G = H / Hkv;
+  const long long rows = B > 0 ? q_start[B] : 0;
+  const long long n_out = rows * H;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (long long i = 0; i < n_out; ++i) {
+    int tid = 0;
+#ifdef _OPENMP
+    tid = omp_get_thread_num();
+#endif
+    double *lg = logit_scratch + (size_t)tid * max_seq_len;
+    const long long row = i / H;
+    const int h = (int)(i % H), kvh = h / G;
+    int s = 0;
+    while (s + 1 < B && q_start[s + 1] <= row) ++s;  /* the row's sequence */
+    const int L = seq_lens[s], n = q_start[s + 1] - q_start[s];
+    const int pos = L - n + (int)(row - q_start[s]);  /* last visible token */
+    double *o = out + (size_t)i * D;
+    for (int d = 0; d < D; ++d) o[d] = 0.0;
+    if (n > L || pos < 0) continue;
+    double m = -INFINITY;
+    for (int t = 0; t <= pos; ++t) {
+      double dot = 0.0;
+      for (int d = 0; d < D; ++d)
+        dot += load_elem(q, (size_t)i * D + d, dtype) *
+               load_elem(k_cache, kv_index(block_tables, s, t, kvh, d, Hkv, D, bs, max_blocks),
+                         dtype);
+      lg[t] = scale * dot;
+      if (lg[t] > m) m = lg[t];
+    }
+    double sum = 0.0;
+    for (int t = 0; t <= pos; ++t) {
+      const double w = exp(lg[t] - m);
+      sum += w;
+      for (int d = 0; d < D; ++d)
+        o[d] += w * load_elem(v_cache, kv_index(block_tables, s, t, kvh, d, Hkv, D, bs, max_blocks),
+                              dtype);
+    }
+    for (int d = 0; d < D; ++d) o[d] = o[d] / sum;
+  }
+}

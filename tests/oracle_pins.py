@@ -292,6 +292,60 @@ def pin_empty_sequence(lib):
     assert np.array_equal(out[0], np.zeros_like(out[0]))
 
 
+def _chunks_case(seed, lens, qlens, H=4, Hkv=2, D=4, bs=4, dtype=torch.float64):
+    """A cache case plus query chunks: rows = sum(qlens) query vectors."""
+    c = small_case(seed, B=len(lens), H=H, Hkv=Hkv, D=D, bs=bs, lens=lens, dtype=dtype)
+    g = torch.Generator().manual_seed(seed + 1000)
+    q = torch.randn(sum(qlens), H, D, generator=g, dtype=torch.float64).to(dtype)
+    q_start = [0]
+    for n in qlens:
+        q_start.append(q_start[-1] + n)
+    return c, q, q_start
+
+
+def pin_query_chunks_single_token_is_decode(lib):
+    """One query token per sequence: the chunk definition is the decode one
+    (computed by the separately pinned attention function)."""
+    c = small_case(31, lens=(1, 6, 17))
+    out = oracle.query_chunks(c.query, c.key_cache, c.value_cache, c.block_tables,
+                              c.seq_lens, [0, 1, 2, 3], c.scale, lib=lib)
+    assert np.allclose(out, _run(lib, c), rtol=0, atol=1e-13)
+
+
+def pin_query_chunks_causal_brute_force(lib):
+    """Chunks of 1, 2, 3 and L tokens against a Python gather and
+    torch.softmax in float64: row i of a chunk of n over L cached tokens
+    sees tokens [0, L - n + i]."""
+    lens, qlens = (5, 7, 9, 4), (1, 2, 3, 4)
+    c, q, qs = _chunks_case(32, lens, qlens)
+    out = oracle.query_chunks(q, c.key_cache, c.value_cache, c.block_tables, c.seq_lens, qs,
+                              c.scale, lib=lib)
+    G = 4 // 2
+    for s, (L, n) in enumerate(zip(lens, qlens)):
+        for i in range(n):
+            for h in range(4):
+                K, V = gather_contiguous(None, c.key_cache, c.value_cache, c.block_tables,
+                                         c.seq_lens, s, h // G)
+                vis = L - n + i + 1
+                w = torch.softmax(c.scale * (K[:vis] @ q[qs[s] + i, h].to(torch.float64)), 0)
+                ref = (w[:, None] * V[:vis]).sum(0)
+                assert torch.allclose(torch.from_numpy(out[qs[s] + i, h]), ref, atol=1e-13)
+
+
+def pin_query_chunks_first_token_sees_itself(lib):
+    """A chunk that is the whole sequence (no prefix): its first token sees
+    only itself, so its output is V_0 exactly; its last token sees all."""
+    lens = (6, 3)
+    c, q, qs = _chunks_case(33, lens, lens)
+    out = oracle.query_chunks(q, c.key_cache, c.value_cache, c.block_tables, c.seq_lens, qs,
+                              c.scale, lib=lib)
+    for s in range(2):
+        for h in range(4):
+            K, V = gather_contiguous(None, c.key_cache, c.value_cache, c.block_tables,
+                                     c.seq_lens, s, h // 2)
+            assert np.array_equal(out[qs[s], h], V[0].numpy())
+
+
 ALL_PINS = [
     pin_hand_examples, pin_widen_bf16, pin_widen_f16, pin_brute_force_softmax,
     pin_sdpa_identity_table, pin_single_token, pin_constant_v,
@@ -299,4 +353,6 @@ ALL_PINS = [
     pin_scale_folds_into_query, pin_gqa_head_map, pin_tail_masking,
     pin_pool_permutation, pin_partition_combine_equals_softmax,
     pin_partials_closed_form, pin_empty_sequence,
+    pin_query_chunks_single_token_is_decode, pin_query_chunks_causal_brute_force,
+    pin_query_chunks_first_token_sees_itself,
 ]

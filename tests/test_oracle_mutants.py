@@ -38,6 +38,12 @@ MUTANTS = [
      "total += exp(ml[p] - gmax) * es[p];", "total += exp(ml[p] - gmax);"),
     ("partition_end_off_by_one", "int t1 = t0 + P < L ? t0 + P : L;",
      "int t1 = t0 + P - 1 < L ? t0 + P - 1 : L;"),
+    ("chunk_sees_one_token_too_many", "const int pos = L - n + (int)(row - q_start[s]);",
+     "const int pos = L - n + (int)(row - q_start[s]) + 1;"),
+    ("chunk_row_to_sequence_off", "while (s + 1 < B && q_start[s + 1] <= row) ++s;",
+     "while (s + 1 < B && q_start[s + 1] < row) ++s;"),
+    ("chunk_query_head_dropped", "dot += load_elem(q, (size_t)i * D + d, dtype) *",
+     "dot += load_elem(q, (size_t)row * H * D + d, dtype) *"),
     ("f16_exponent_bias", "e - 25); /* (1 + f/1024)", "e - 24); /* (1 + f/1024)"),
     ("f16_subnormal_scale", "ldexp((double)f, -24)", "ldexp((double)f, -25)"),
     ("bf16_wrong_half", "uint32_t u = (uint32_t)b << 16;", "uint32_t u = (uint32_t)b << 15;"),
