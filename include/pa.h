@@ -164,6 +164,38 @@ pa_status_t pa_forward(void *out, const void *query, const void *key_cache,
                        void *workspace, size_t workspace_bytes, void *stream,
                        const pa_options_t *opts);
 
+/* Multi-token queries over the paged cache: the query of sequence s is a
+ * chunk of its LAST n_s = q_start[s+1] - q_start[s] cached tokens (for
+ * example draft tokens to verify, or a small prefill chunk whose keys and
+ * values are already in the cache), rows q_start[s] .. q_start[s+1]-1 of
+ * query and out ([num_rows][num_heads][head_size]).  Chunk token i, at cache
+ * position L - n_s + i with L = seq_lens[s], attends causally to the cache
+ * tokens [0, L - n_s + i].  The pages give no formula for this; it is the
+ * plain causal reading of attention over a paged prefix (the prefill patch
+ * of project_6 tunes such a kernel).
+ *
+ * q_start: device int32 [num_seqs + 1], non-decreasing, q_start[0] = 0,
+ * q_start[num_seqs] = num_rows, 0 <= n_s <= min(seq_lens[s], max_chunk).
+ * The other arguments as pa_forward (opts->variant picks V1/V2/auto); the V2
+ * workspace is sized as pa_workspace_bytes(num_rows, ...).  bf16 and f16 only
+ * (PA_ERR_UNSUPPORTED for f32).  An item covers 16 / (num_heads /
+ * num_kv_heads) tokens of a chunk, so longer chunks re-read their prefix once
+ * per such group (from L2 when the groups of a partition run together).  A
+ * chunk that breaks the rules above is reported as PA_ERR_DEVICE_BAD_INPUT
+ * and its rows hold no meaningful values (the other sequences' rows are
+ * computed as usual). */
+pa_status_t pa_chunks_forward(void *out, const void *query,
+                              const void *key_cache, const void *value_cache,
+                              const int32_t *block_tables,
+                              const int32_t *seq_lens, const int32_t *q_start,
+                              int num_seqs, int num_rows, int max_chunk,
+                              int num_heads, int num_kv_heads, int head_size,
+                              int num_blocks, int block_size,
+                              int max_blocks_per_seq, int max_seq_len,
+                              float scale, int partition_size, int dtype,
+                              void *workspace, size_t workspace_bytes,
+                              void *stream, const pa_options_t *opts);
+
 /* Device bytes of the staging buffer pa_forward_host needs: the query and
  * the output ([num_seqs][num_heads][head_size] in the dtype), the block
  * tables and seq_lens, each part 256-byte aligned.  Returns 0 on bad

@@ -42,7 +42,8 @@ _DTYPES = {torch.float32: PA_DTYPE_F32, torch.bfloat16: PA_DTYPE_BF16,
 EXPORTS = ("pa_workspace_bytes", "pa_workspace_layout", "pa_workspace_init",
            "pa_v1_forward", "pa_v2_forward", "pa_forward", "pa_choose_v2",
            "pa_read_device_status", "pa_status_string", "pa_last_cuda_error",
-           "pa_version", "pa_v2_forward_noalloc", "pa_host_staging_bytes", "pa_forward_host")
+           "pa_version", "pa_v2_forward_noalloc", "pa_host_staging_bytes", "pa_forward_host",
+           "pa_chunks_forward")
 
 
 class PAError(RuntimeError):
@@ -92,6 +93,10 @@ def load_library(path: str = LIB_PATH):
         lib.pa_v2_forward_noalloc.argtypes = _FWD_ARGS[:17] + [vp]
         lib.pa_forward.restype = ci
         lib.pa_forward.argtypes = _FWD_ARGS + [ctypes.POINTER(pa_options_t)]
+        lib.pa_chunks_forward.restype = ci
+        lib.pa_chunks_forward.argtypes = ([vp] * 7 + [ci] * 10 +
+                                          [ctypes.c_float, ci, ci, vp, cs, vp,
+                                           ctypes.POINTER(pa_options_t)])
         lib.pa_host_staging_bytes.restype = cs
         lib.pa_host_staging_bytes.argtypes = [ci] * 5
         lib.pa_forward_host.restype = ci
@@ -232,6 +237,32 @@ def pa_forward(out, query, key_cache, value_cache, block_tables, seq_lens, scale
     _check(load_library().pa_forward(*_fwd_args(
         out, query, key_cache, value_cache, block_tables, seq_lens, scale, partition_size,
         workspace, max_seq_len, stream), ctypes.byref(opts)), "pa_forward")
+
+
+def pa_chunks_forward(out, query, key_cache, value_cache, block_tables, seq_lens, q_start,
+                      scale, partition_size, workspace, max_seq_len=None, max_chunk=None,
+                      stream=None, variant=PA_VARIANT_AUTO, num_stages=0, ctas_per_sm=0) -> None:
+    """Multi-token queries over the paged cache (see include/pa.h): query and
+    out [num_rows, H, D]; the chunk of sequence s is rows q_start[s] ..
+    q_start[s+1]-1 (int32 on the device), its last tokens.  max_chunk bounds
+    the chunk lengths (default: max_seq_len)."""
+    if query.dtype not in _DTYPES:
+        raise ValueError(f"unsupported dtype {query.dtype}")
+    R, H, D = query.shape
+    nb, hkv, bs, d2 = key_cache.shape
+    B = seq_lens.numel()
+    if q_start.numel() != B + 1 or q_start.dtype != torch.int32:
+        raise ValueError("q_start must be int32 [num_seqs + 1]")
+    if max_seq_len is None:
+        max_seq_len = block_tables.shape[1] * bs
+    mc = int(max_chunk) if max_chunk is not None else int(max_seq_len)
+    opts = pa_options_t(variant, PA_MATH_AUTO, num_stages, 0, 0, None, ctas_per_sm, 0)
+    _check(load_library().pa_chunks_forward(
+        _ptr(out), _ptr(query), _ptr(key_cache), _ptr(value_cache), _ptr(block_tables),
+        _ptr(seq_lens), _ptr(q_start), B, R, mc, H, hkv, D, nb, bs, block_tables.shape[1],
+        int(max_seq_len), float(scale), int(partition_size), _DTYPES[query.dtype],
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream_handle(stream),
+        ctypes.byref(opts)), "pa_chunks_forward")
 
 
 def pa_host_staging_bytes(num_seqs: int, num_heads: int, head_size: int,

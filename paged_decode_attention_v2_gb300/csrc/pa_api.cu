@@ -183,7 +183,19 @@ struct Call {
   void *workspace;
   size_t workspace_bytes;
   cudaStream_t stream;
+  // query chunks (pa_chunks_forward); q_start == nullptr: one query a sequence
+  const int32_t *q_start;
+  int num_rows;
+  int max_chunk;
 };
+
+// Rows of query (and output) and of the V2 workspace: sequences, or the query
+// chunks' rows.
+int query_rows(const Call &c) { return c.q_start ? c.num_rows : c.num_seqs; }
+
+// Chunk mode: tokens of one item (its (token, head) rows fill the 16 columns
+// of the two-n-tile tensor path).
+int chunk_tokens_of(const Call &c) { return 16 / (c.num_heads / c.num_kv_heads); }
 
 int max_parts_of(int max_seq_len, int partition_size) {
   return (max_seq_len + partition_size - 1) / partition_size;
@@ -210,8 +222,15 @@ pa_status_t check_args(const Call &c, bool need_v2) {
     return PA_ERR_UNSUPPORTED;
   if ((long long)c.num_blocks * c.num_kv_heads * c.block_size >= (1ll << 31))
     return PA_ERR_UNSUPPORTED;
-  if ((long long)c.num_seqs * c.num_kv_heads * max_parts_of(c.max_seq_len, c.partition_size) >=
-      (1ll << 31))
+  if (c.q_start) {
+    if (c.num_rows < 0 || c.max_chunk < 1 || c.max_chunk > c.max_seq_len) return PA_ERR_INVALID_ARG;
+    if (c.dtype == PA_DTYPE_F32) return PA_ERR_UNSUPPORTED;  // tensor path only
+    if (!aligned(c.q_start, 4)) return PA_ERR_INVALID_ARG;
+  }
+  const long long groups =
+      c.q_start ? (c.max_chunk + chunk_tokens_of(c) - 1) / chunk_tokens_of(c) : 1;
+  if ((long long)c.num_seqs * c.num_kv_heads * max_parts_of(c.max_seq_len, c.partition_size) *
+          groups >= (1ll << 31))
     return PA_ERR_UNSUPPORTED;
   if (need_v2 && max_parts_of(c.max_seq_len, c.partition_size) > kMaxReduceParts)
     return PA_ERR_UNSUPPORTED;
@@ -222,7 +241,7 @@ pa_status_t check_args(const Call &c, bool need_v2) {
       !aligned(c.value_cache, 16) || !aligned(c.block_tables, 4) || !aligned(c.seq_lens, 4) ||
       !aligned(c.workspace, 256))
     return PA_ERR_INVALID_ARG;
-  const size_t need = need_v2 ? pa_workspace_bytes(c.num_seqs, c.num_heads, c.head_size,
+  const size_t need = need_v2 ? pa_workspace_bytes(query_rows(c), c.num_heads, c.head_size,
                                                    c.max_seq_len, c.partition_size)
                               : (size_t)kStatusBytes;
   if (need == 0) return PA_ERR_INVALID_ARG;
@@ -261,7 +280,12 @@ pa_status_t launch(const Call &c, bool v2, const pa_options_t &opt) {
   if (math == PA_MATH_AUTO) math = c.dtype == PA_DTYPE_F32 ? kMathSimt : kMathTensor;
   if (math != kMathSimt && math != kMathTensor) return PA_ERR_INVALID_ARG;
   if (math == kMathTensor && c.dtype == PA_DTYPE_F32) return PA_ERR_UNSUPPORTED;
-  const AttnKernelInfo k = pick_kernel(math, c.dtype, c.head_size, group);
+  const bool chunk = c.q_start != nullptr;
+  if (chunk && math != kMathTensor) return PA_ERR_UNSUPPORTED;
+  const AttnKernelInfo k =
+      chunk ? (c.dtype == PA_DTYPE_BF16 ? attn_kernel_chunk_bf16(c.head_size)
+                                        : attn_kernel_chunk_f16(c.head_size))
+            : pick_kernel(math, c.dtype, c.head_size, group);
   if (!k.fn) return PA_ERR_UNSUPPORTED;
 
   const int elt = elt_size(c.dtype);
@@ -288,7 +312,7 @@ pa_status_t launch(const Call &c, bool v2, const pa_options_t &opt) {
   const int max_parts = v2 ? max_parts_of(c.max_seq_len, c.partition_size) : 1;
   size_t off[5] = {0, 0, 0, 0, 0};
   if (v2) {
-    if (pa_workspace_layout(c.num_seqs, c.num_heads, c.head_size, c.max_seq_len,
+    if (pa_workspace_layout(query_rows(c), c.num_heads, c.head_size, c.max_seq_len,
                             c.partition_size, off) != PA_OK)
       return PA_ERR_INVALID_ARG;
   }
@@ -326,6 +350,16 @@ pa_status_t launch(const Call &c, bool v2, const pa_options_t &opt) {
     const int fuse = opt.fuse_partitions > 0 ? opt.fuse_partitions : 0;
     p.fuse_limit = fuse > kFuseLimitMax ? kFuseLimitMax : fuse;
     p.group_count = reinterpret_cast<int *>(ws + off[4]);
+    // chunk mode: no fused combine; the counters region holds the rows' limits
+    if (chunk) {
+      p.fuse_limit = 0;
+      p.row_limit = reinterpret_cast<int *>(ws + off[4]);
+    }
+  }
+  if (chunk) {
+    p.q_start = c.q_start;
+    p.num_rows = c.num_rows;
+    p.chunk_tokens = chunk_tokens_of(c);
   }
   p.num_stages = stages;
   p.debug_flags = opt.debug_flags;
@@ -343,7 +377,8 @@ pa_status_t launch(const Call &c, bool v2, const pa_options_t &opt) {
   if (st != PA_OK) return st;
   if (per_sm < 1) return PA_ERR_UNSUPPORTED;
   if (opt.ctas_per_sm > 0 && opt.ctas_per_sm < per_sm) per_sm = opt.ctas_per_sm;
-  const long long max_items = (long long)c.num_seqs * c.num_kv_heads * p.max_parts;
+  const long long max_items = (long long)c.num_seqs * c.num_kv_heads * p.max_parts *
+                              (chunk ? (c.max_chunk + p.chunk_tokens - 1) / p.chunk_tokens : 1);
   long long grid = (long long)per_sm * dev->sm_count;
   if (grid > max_items) grid = max_items;
   if (grid > 0) {
@@ -384,20 +419,21 @@ pa_status_t launch(const Call &c, bool v2, const pa_options_t &opt) {
   r.tmp_out = p.tmp_out;
   r.seq_lens = c.seq_lens;
   r.status = p.status;
-  r.num_seqs = c.num_seqs;
+  r.num_seqs = query_rows(c);  // Phase 2 rows: (query row, head)
   r.num_heads = c.num_heads;
   r.head_size = c.head_size;
   r.max_parts = p.max_parts;
   r.partition_size = c.partition_size;
   r.max_seq_len = c.max_seq_len;
   r.fuse_limit = p.fuse_limit;
+  r.row_limit = p.row_limit;
   // Team size W (warps per task) and column split: the pair that minimises
   // the chain of the longest task (1 + its rounds of loads, a round being one
   // batch of NB partitions per thread) plus 2 for every further wave of
   // tasks (the typical task, with sequences of mixed lengths, takes one
   // round).  Only max_seq_len is known here, so the longest task is sized
   // from it.
-  const long long prows = (long long)c.num_seqs * c.num_heads;
+  const long long prows = (long long)query_rows(c) * c.num_heads;
   if (prows == 0) return PA_OK;
   int occ = 0;
   {
@@ -585,6 +621,29 @@ pa_status_t pa_forward(void *out, const void *query, const void *key_cache,
                        max_blocks_per_seq, max_seq_len, scale, partition_size, dtype, workspace,
                        workspace_bytes, stream),
              opt.variant, opt);
+}
+
+pa_status_t pa_chunks_forward(void *out, const void *query, const void *key_cache,
+                              const void *value_cache, const int32_t *block_tables,
+                              const int32_t *seq_lens, const int32_t *q_start, int num_seqs,
+                              int num_rows, int max_chunk, int num_heads, int num_kv_heads,
+                              int head_size, int num_blocks, int block_size,
+                              int max_blocks_per_seq, int max_seq_len, float scale,
+                              int partition_size, int dtype, void *workspace,
+                              size_t workspace_bytes, void *stream, const pa_options_t *opts) {
+  if (!q_start) return PA_ERR_INVALID_ARG;
+  pa_options_t opt;
+  memset(&opt, 0, sizeof opt);
+  if (opts) opt = *opts;
+  Call c = make_call(out, query, key_cache, value_cache, block_tables, seq_lens, num_seqs,
+                     num_heads, num_kv_heads, head_size, num_blocks, block_size,
+                     max_blocks_per_seq, max_seq_len, scale, partition_size, dtype, workspace,
+                     workspace_bytes, stream);
+  c.q_start = q_start;
+  c.num_rows = num_rows;
+  c.max_chunk = max_chunk;
+  if (num_rows == 0) return check_args(c, false);
+  return run(c, opt.variant, opt);
 }
 
 size_t pa_host_staging_bytes(int num_seqs, int num_heads, int head_size,

@@ -95,23 +95,38 @@ struct StageGeom {
 // Accumulation is fp32.  P is rounded to the input type for the PV product
 // and the running sum adds the rounded values, so the weights used and the
 // normaliser agree.
-template <typename T, int D, int NT>
+template <typename T, int D, int NT, bool CHUNK = false>
 struct TensorMath {
   static constexpr int KS = D / 16;
   static constexpr int GMAX = 8 * NT;
+  // Query chunks (several tokens of a sequence per item, causal among them):
+  // the columns are (token, head) rows, each with its own key limit.
+  static constexpr bool kChunk = CHUNK;
   uint32_t qf[NT][KS][2];
   float o[NT][KS][4];
   float m[NT][2];
   float l[NT][2];
+  int lim[CHUNK ? NT : 1][2];  // chunk mode: keys at or past lim[..] are hidden
 
-  // Start an item: queries of the group from shared memory ([G][D], input
-  // type), fresh softmax state.
-  __device__ __forceinline__ void begin_item(const uint8_t *q_smem, int group, int lane, int) {
+  // Start an item: queries of the group from shared memory ([rows][D], input
+  // type), fresh softmax state.  Chunk mode: row r belongs to the item's
+  // (r / group)-th token, which sees the keys below lim_base + r / group + 1.
+  __device__ __forceinline__ void begin_item(const uint8_t *q_smem, int rows, int lane, int,
+                                             int lim_base = 0, int group = 1) {
     const T *q = reinterpret_cast<const T *>(q_smem);
+    if constexpr (CHUNK) {
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const int c = nt * 8 + 2 * (lane & 3) + j;  // this thread's S^T columns
+          lim[nt][j] = c < rows ? lim_base + c / group + 1 : 0x7fffffff;
+        }
+    }
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       const int h = nt * 8 + (lane >> 2);
-      const bool live = h < group;
+      const bool live = h < rows;
 #pragma unroll
       for (int ks = 0; ks < KS; ++ks) {
         const T *src = q + h * D + ks * 16 + 2 * (lane & 3);
@@ -130,7 +145,7 @@ struct TensorMath {
   __device__ __forceinline__ void bind(float *, float *) {}
 
   __device__ __forceinline__ void tile(uint32_t kbase, uint32_t vbase, const StageGeom &g, int tok0,
-                                       int valid, int lane, float scale_log2) {
+                                       int valid, int lane, float scale_log2, int abs0 = 0) {
     const int mi = lane >> 3, r = lane & 7;
     // ---- S^T = K Q^T
     // Two accumulators per n-tile (even / odd k-steps) halve the chain of
@@ -169,16 +184,27 @@ struct TensorMath {
       float x2 = sacc[nt][2] * scale_log2, x3 = sacc[nt][3] * scale_log2;
       if (t_lo >= valid) x0 = x1 = -CUDART_INF_F;
       if (t_hi >= valid) x2 = x3 = -CUDART_INF_F;
+      if constexpr (CHUNK) {  // causal limits of the (token, head) columns
+        const int k_lo = abs0 + t_lo, k_hi = abs0 + t_hi;
+        if (k_lo >= lim[nt][0]) x0 = -CUDART_INF_F;
+        if (k_lo >= lim[nt][1]) x1 = -CUDART_INF_F;
+        if (k_hi >= lim[nt][0]) x2 = -CUDART_INF_F;
+        if (k_hi >= lim[nt][1]) x3 = -CUDART_INF_F;
+      }
       float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
 #pragma unroll
       for (int off = 4; off < 32; off <<= 1) {
         mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
         mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
       }
-      const float mn0 = fmaxf(m[nt][0], mx0), mn1 = fmaxf(m[nt][1], mx1);
-      const float al0 = exp2f(m[nt][0] - mn0), al1 = exp2f(m[nt][1] - mn1);
-      const uint32_t plo = MmaOp<T>::pack(exp2f(x0 - mn0), exp2f(x1 - mn1));
-      const uint32_t phi = MmaOp<T>::pack(exp2f(x2 - mn0), exp2f(x3 - mn1));
+      float mn0 = fmaxf(m[nt][0], mx0), mn1 = fmaxf(m[nt][1], mx1);
+      // chunk mode: a column that has seen no key yet keeps m = -inf; take
+      // its exponents against 0 so that they come out 0, not NaN
+      const float mb0 = CHUNK && mn0 == -CUDART_INF_F ? 0.f : mn0;
+      const float mb1 = CHUNK && mn1 == -CUDART_INF_F ? 0.f : mn1;
+      const float al0 = exp2f(m[nt][0] - mb0), al1 = exp2f(m[nt][1] - mb1);
+      const uint32_t plo = MmaOp<T>::pack(exp2f(x0 - mb0), exp2f(x1 - mb1));
+      const uint32_t phi = MmaOp<T>::pack(exp2f(x2 - mb0), exp2f(x3 - mb1));
       const float2 flo = MmaOp<T>::unpack(plo), fhi = MmaOp<T>::unpack(phi);
       l[nt][0] = l[nt][0] * al0 + (flo.x + fhi.x);
       l[nt][1] = l[nt][1] * al1 + (flo.y + fhi.y);
@@ -256,6 +282,9 @@ struct TensorMath {
         float L = 0.f;
         for (int w = 0; w < nw; ++w) L += l_s[w * GMAX + h] * exp2f(m_s[w * GMAX + h] - M);
         f[j] = exp2f(m[nt][j] - M) / L;  // 0 for a warp that saw no token
+        if constexpr (CHUNK) {
+          if (!(L > 0.f)) f[j] = 0.f;  // a column that saw no key at all: zeros
+        }
       }
       const int h0 = nt * 8 + 2 * (lane & 3);
 #pragma unroll
@@ -278,6 +307,7 @@ struct TensorMath {
 // reads the tile's probabilities from a small shared-memory table.
 template <typename T, int D, int GMAX>
 struct SimtMath {
+  static constexpr bool kChunk = false;  // query chunks run on the tensor path only
   static constexpr int ELT = sizeof(T);
   static constexpr int CPR = D * ELT / 16;  // 16-byte chunks per row
   static constexpr int EPC = 16 / ELT;      // elements per chunk
@@ -302,7 +332,7 @@ struct SimtMath {
   // input type, in shared memory) into the fp32 table q_s (the caller then
   // synchronises the consumer warps).
   __device__ __forceinline__ void begin_item(const uint8_t *q_smem, int group, int,
-                                             int ncons) {
+                                             int ncons, int = 0, int = 1) {
     const T *q = reinterpret_cast<const T *>(q_smem);
     for (int i = threadIdx.x; i < GMAX * D; i += ncons) {
       const int g = i / D, d = i % D;
@@ -369,7 +399,7 @@ struct SimtMath {
   }
 
   __device__ __forceinline__ void tile(uint32_t kbase, uint32_t vbase, const StageGeom &g, int tok0,
-                                       int valid, int lane, float scale_log2) {
+                                       int valid, int lane, float scale_log2, int = 0) {
     const int tok = lane & 15, half = lane >> 4;
     float dot[GMAX];
 #pragma unroll
@@ -549,6 +579,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) __maxnreg__((kernel_max_regs
     // the cursor (a chunk of 32 sequences, scanned once) only moves forward
     // because every CTA takes items in increasing order.
     int cs = 0, cbase = 0, c_cnt = 0, c_incl = 0, c_L = 0, c_total = 0;
+    int c_qs = 0, c_n = 0, c_nrg = 0;  // chunk mode: first query row, chunk tokens, row groups
     bool c_loaded = false;
     auto load_chunk = [&]() {
       const int sl = cs + lane;
@@ -566,6 +597,23 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) __maxnreg__((kernel_max_regs
       const int c_np = (c_L + p.range_tokens - 1) / p.range_tokens;
       c_cnt = sl >= p.num_seqs ? 0
                                : p.num_kv_heads * (c_np == 0 && p.fuse_limit > 0 ? 1 : c_np);
+      if constexpr (Math::kChunk) {
+        // the sequence's query chunk: its last c_n tokens, query rows from c_qs;
+        // items: (KV head, partition, group of chunk_tokens tokens)
+        c_qs = 0;
+        c_n = 0;
+        if (sl < p.num_seqs) {
+          c_qs = __ldg(p.q_start + sl);
+          const int qe = __ldg(p.q_start + sl + 1);
+          c_n = qe - c_qs;
+          if (c_qs < 0 || c_n < 0 || c_n > c_L || qe > p.num_rows) {
+            report(p.status, kStatusBadInput);  // its rows get no items
+            c_n = 0;
+          }
+        }
+        c_nrg = (c_n + p.chunk_tokens - 1) / p.chunk_tokens;
+        c_cnt = sl >= p.num_seqs ? 0 : p.num_kv_heads * c_np * c_nrg;
+      }
       c_incl = c_cnt;
 #pragma unroll
       for (int off = 1; off < 32; off <<= 1) {
@@ -601,10 +649,11 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) __maxnreg__((kernel_max_regs
     while (true) {
       // ---- locate the item: (s, kvh, part, L)
       int s = 0, kvh = 0, part = 0, L = 0, np_s = 1;
+      int nrg = 0, qs = 0, n_s = 0, rg = 0;  // chunk mode
       bool found = false;
       if (item < 0) {  // a corrupted work counter: stop rather than guess
         if (lane == 0) report(p.status, kStatusBadInput);
-      } else if (!p.write_partials) {  // V1: Hkv items per sequence, empty ones too
+      } else if (!p.write_partials && !Math::kChunk) {  // V1: Hkv items per sequence, empty ones too
         s = item / p.num_kv_heads;
         if (s < p.num_seqs) {
           found = true;
@@ -625,9 +674,22 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) __maxnreg__((kernel_max_regs
             L = __shfl_sync(0xffffffffu, c_L, ls);
             const int first = cbase + __shfl_sync(0xffffffffu, c_incl - c_cnt, ls);
             np_s = (L + p.range_tokens - 1) / p.range_tokens;
-            const int items_per_head = np_s > 0 ? np_s : 1;
-            kvh = (item - first) / items_per_head;
-            part = (item - first) % items_per_head;
+            if constexpr (Math::kChunk) {
+              // (KV head, partition, row group); the row groups of one
+              // partition are neighbours, so their K/V re-reads hit L2
+              nrg = __shfl_sync(0xffffffffu, c_nrg, ls);
+              qs = __shfl_sync(0xffffffffu, c_qs, ls);
+              n_s = __shfl_sync(0xffffffffu, c_n, ls);
+              const int per_head = np_s * nrg;
+              kvh = (item - first) / per_head;
+              const int rem = (item - first) % per_head;
+              part = rem / nrg;
+              rg = rem % nrg;
+            } else {
+              const int items_per_head = np_s > 0 ? np_s : 1;
+              kvh = (item - first) / items_per_head;
+              part = (item - first) % items_per_head;
+            }
             found = s < p.num_seqs;  // always, by the count above; never write past the batch
             break;
           }
@@ -641,7 +703,24 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) __maxnreg__((kernel_max_regs
       const int next_raw = grab_issue();  // its latency overlaps this item's stages
 
       const int tok_begin = part * p.range_tokens;
-      const int tok_end = min(tok_begin + p.range_tokens, L);
+      int tok_end = min(tok_begin + p.range_tokens, L);
+      // chunk mode: the item's tokens, its output rows and key limits
+      int row0 = 0, rows = 0, lim_base = 0, ntok = 0;
+      if constexpr (Math::kChunk) {
+        const int t_first = rg * p.chunk_tokens;
+        ntok = min(p.chunk_tokens, n_s - t_first);
+        rows = ntok * p.group;
+        lim_base = L - n_s + t_first;  // keys below lim_base + i + 1 for token i of the group
+        row0 = qs + t_first;
+        tok_end = min(tok_end, lim_base + ntok);
+        // Phase 2 needs each row's count of visible keys: the partition-0
+        // items (one per KV head, all equal) record it
+        if (part == 0 && lane < ntok && p.row_limit) p.row_limit[row0 + lane] = lim_base + lane + 1;
+        if (tok_end <= tok_begin) {  // the partition lies past every token of the group
+          item = grab_value(next_raw);
+          continue;
+        }
+      }
       if (tok_end <= tok_begin) {  // empty sequence (V1, or V2 with the fused combine): zeros
         T *o = static_cast<T *>(p.out) + ((size_t)s * p.num_heads + (size_t)kvh * p.group) * D;
         for (int e = lane; e < p.group * D; e += 32) o[e] = from_float<T>(0.f);
@@ -693,8 +772,14 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) __maxnreg__((kernel_max_regs
           h.tok_end = tok_end;
           h.flags = (first ? kStageFirst : 0) | (j == n_st - 1 ? kStageLast : 0);
           h.np = np_s;
+          const uint32_t q_in = Math::kChunk ? (uint32_t)(ntok * qbytes) : (uint32_t)qbytes;
+          if constexpr (Math::kChunk) {
+            h.s = row0;     // first output row
+            h.np = rows;    // (token, head) rows
+            h.pad = lim_base;
+          }
           mbar_arrive_expect_tx(full0 + 8 * st, (uint32_t)__popc(valid_mask) * U * ROW_BYTES * 2 +
-                                                    (first ? (uint32_t)qbytes : 0u));
+                                                    (first ? q_in : 0u));
         }
         __syncwarp();
         if (y >= 0) {
@@ -708,7 +793,14 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) __maxnreg__((kernel_max_regs
                              full0 + 8 * st, kv_policy);
           }
         }
-        if (first && lane == 0) {
+        if constexpr (Math::kChunk) {
+          if (first && lane < ntok) {  // one copy per token: its G heads are contiguous
+            const T *q = static_cast<const T *>(p.query) +
+                         ((size_t)(row0 + lane) * p.num_heads + (size_t)kvh * p.group) * D;
+            bulk_load(qbuf_u32 + (uint32_t)st * QBYTES + (uint32_t)(lane * qbytes), q,
+                      (uint32_t)qbytes, full0 + 8 * st);
+          }
+        } else if (first && lane == 0) {
           const T *q = static_cast<const T *>(p.query) +
                        ((size_t)s * p.num_heads + (size_t)kvh * p.group) * D;
           bulk_load(qbuf_u32 + (uint32_t)st * QBYTES, q, (uint32_t)qbytes, full0 + 8 * st);
@@ -776,7 +868,10 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) __maxnreg__((kernel_max_regs
       const StageInfo h = info[st];
       if (h.flags & kStageEnd) break;
       if (h.flags & kStageFirst) {
-        math.begin_item(qbuf + (size_t)st * QBYTES, p.group, lane, NCONS);
+        if constexpr (Math::kChunk)  // rows = (token, head) pairs; h.pad = first token's key limit
+          math.begin_item(qbuf + (size_t)st * QBYTES, h.np, lane, NCONS, h.pad, p.group);
+        else
+          math.begin_item(qbuf + (size_t)st * QBYTES, p.group, lane, NCONS);
         if constexpr (SIMT) {
           ok = cons_sync();  // the shared fp32 query table is complete
           if (!ok) break;
@@ -786,7 +881,8 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) __maxnreg__((kernel_max_regs
       const int valid = max(0, min(kTileTokens, h.tok_end - tile_tok0));
       if (valid > 0) {
         const uint32_t kbase = ring_u32 + (uint32_t)st * 2 * HALF_BYTES;
-        math.tile(kbase, kbase + HALF_BYTES, geom, warp * kTileTokens, valid, lane, p.scale_log2);
+        math.tile(kbase, kbase + HALF_BYTES, geom, warp * kTileTokens, valid, lane, p.scale_log2,
+                  tile_tok0);
       }
       __syncwarp();
       if (!(h.flags & kStageLast)) {
@@ -810,8 +906,14 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) __maxnreg__((kernel_max_regs
       // out[h][d] = sum over warps of the scaled partial outputs (16 bytes a thread)
       const int G = p.group;
       const size_t head0 = (size_t)h.s * p.num_heads + (size_t)h.kvh * G;
-      for (int idx = threadIdx.x; idx < G * (D / 4); idx += NCONS) {
+      // output rows of the item: the group's G heads, or in chunk mode h.np
+      // (token, head) rows starting at query row h.s
+      const int rows = Math::kChunk ? h.np : G;
+      for (int idx = threadIdx.x; idx < rows * (D / 4); idx += NCONS) {
         const int hh = idx / (D / 4), d = 4 * (idx % (D / 4));
+        const size_t orow = Math::kChunk ? ((size_t)h.s + hh / G) * p.num_heads +
+                                               (size_t)h.kvh * G + hh % G
+                                         : head0 + hh;
         float4 acc = *reinterpret_cast<const float4 *>(&o_s[(size_t)hh * (D + 4) + d]);
 #pragma unroll
         for (int w2 = 1; w2 < NW; ++w2) {
@@ -823,7 +925,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) __maxnreg__((kernel_max_regs
           acc.w += v.w;
         }
         if (p.write_partials) {
-          const size_t row = (head0 + hh) * p.max_parts + h.part;
+          const size_t row = orow * p.max_parts + h.part;
           *reinterpret_cast<float4 *>(p.tmp_out + row * D + d) = acc;
           if (d == 0) {
             float M = -CUDART_INF_F;
@@ -836,14 +938,14 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) __maxnreg__((kernel_max_regs
             p.exp_sums[row] = L;
           }
         } else {
-          T *o = static_cast<T *>(p.out) + (head0 + hh) * D + d;
+          T *o = static_cast<T *>(p.out) + orow * D + d;
           o[0] = from_float<T>(acc.x);
           o[1] = from_float<T>(acc.y);
           o[2] = from_float<T>(acc.z);
           o[3] = from_float<T>(acc.w);
         }
       }
-      if (p.write_partials && h.np <= p.fuse_limit) {
+      if (!Math::kChunk && p.write_partials && h.np <= p.fuse_limit) {
         // Phase 2 inside Phase 1 for a sequence of few partitions: the last
         // CTA to finish one of them (per KV head) combines them all, with the
         // same log-sum-exp rule as the Phase 2 kernel.
@@ -974,6 +1076,17 @@ AttnKernelInfo select_tensor(int D, int group) {
       case 128: return attn_info<T, 128, consumer_warps<T, 128>(), 16, TensorMath<T, 128, 2>, false>();
       case 256: return attn_info<T, 256, consumer_warps<T, 256>(), 16, TensorMath<T, 256, 2>, false>();
     }
+  }
+  return AttnKernelInfo{nullptr, 0, 0, 0};
+}
+
+// Query chunks: the two-n-tile tensor path, 16 (token, head) rows an item.
+template <typename T>
+AttnKernelInfo select_chunk(int D) {
+  switch (D) {
+    case 64: return attn_info<T, 64, consumer_warps<T, 64>(), 16, TensorMath<T, 64, 2, true>, false>();
+    case 128: return attn_info<T, 128, consumer_warps<T, 128>(), 16, TensorMath<T, 128, 2, true>, false>();
+    case 256: return attn_info<T, 256, consumer_warps<T, 256>(), 16, TensorMath<T, 256, 2, true>, false>();
   }
   return AttnKernelInfo{nullptr, 0, 0, 0};
 }

@@ -1,0 +1,8 @@
+// Instantiations of the attention kernel for query chunks: tensor math, f16 elements.
+#include "pa_attn.cuh"
+
+namespace pa {
+
+AttnKernelInfo attn_kernel_chunk_f16(int head_size) { return select_chunk<__half>(head_size); }
+
+}  // namespace pa

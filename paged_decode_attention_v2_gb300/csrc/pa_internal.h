@@ -35,6 +35,14 @@ struct AttnParams {
   int fuse_limit;     // V2: sequences of at most this many partitions get the
                       // cross-partition combine inside this kernel (0 = none)
   int *group_count;   // V2 fused combine: finished partitions per (seq, kv head)
+  // Query chunks (pa_chunks_forward): the chunk of sequence s is query rows
+  // q_start[s] .. q_start[s+1]-1, its last tokens; an item takes up to
+  // chunk_tokens of them (x group rows <= 16).  Null q_start: one query per
+  // sequence.
+  const int32_t *q_start;
+  int num_rows;
+  int chunk_tokens;
+  int *row_limit;     // V2 chunk mode: keys visible to each query row (for Phase 2)
   int num_stages;
   int debug_flags;
   float scale_log2;   // scale * log2(e)
@@ -50,6 +58,8 @@ struct ReduceParams {
   int num_seqs, num_heads, head_size, max_parts, partition_size, max_seq_len;
   int fuse_limit;      // sequences of at most this many partitions were
                        // finished by Phase 1 (0 = none)
+  const int *row_limit; // chunk mode: keys visible to each query row (null: the
+                        // sequence's length, rows being sequences)
   int cols_per_cta;    // columns of one task: head_size / (column split)
   int warps_per_head;  // warps of the team that serves one task: 1, 2, 4 or 8
 };
@@ -94,6 +104,8 @@ AttnKernelInfo attn_kernel_tensor_f16(int head_size, int group);
 AttnKernelInfo attn_kernel_simt_f32(int head_size, int group);
 AttnKernelInfo attn_kernel_simt_bf16(int head_size, int group);
 AttnKernelInfo attn_kernel_simt_f16(int head_size, int group);
+AttnKernelInfo attn_kernel_chunk_bf16(int head_size);
+AttnKernelInfo attn_kernel_chunk_f16(int head_size);
 const void *reduce_kernel(int dtype, int float4_per_thread);
 
 }  // namespace pa

@@ -55,6 +55,10 @@ __device__ __forceinline__ void team_sync(int g, int nthreads) {
 }
 
 __device__ __forceinline__ int partitions_of(const ReduceParams &p, long long row) {
+  if (p.row_limit) {  // query chunks: the row's own visible keys (a Phase 1 result)
+    const int Lr = __ldcg(p.row_limit + row / p.num_heads);
+    return (Lr + p.partition_size - 1) / p.partition_size;
+  }
   int L = __ldg(p.seq_lens + row / p.num_heads);
   L = L < 0 ? 0 : (L > p.max_seq_len ? p.max_seq_len : L);  // Phase 1 reported it
   return (L + p.partition_size - 1) / p.partition_size;
@@ -85,8 +89,10 @@ __global__ void __launch_bounds__(kReduceThreads, 4)
   // seq_lens is an input, not a Phase 1 result: read the first task's before
   // waiting for Phase 1 (programmatic dependent launch), later ones a task
   // ahead.
-  int np_next = task < ntasks ? partitions_of(p, task / dsplit) : 0;
+  // (in chunk mode the counts are Phase 1 results: read after the wait)
+  int np_next = task < ntasks && !p.row_limit ? partitions_of(p, task / dsplit) : 0;
   pdl_wait_primary();
+  if (p.row_limit && task < ntasks) np_next = partitions_of(p, task / dsplit);
   pdl_launch_dependents();  // the next kernel still waits for this grid to complete
 
   for (; task < ntasks; task += tstride) {
