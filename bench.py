@@ -45,6 +45,7 @@ METRIC = "paged decode attention KV-read GB/s (% of GB300 HBM peak) and decode t
 UNIT = "GB/s"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
+CHUNK_TOKENS = 4
 SECONDARY = "c3_long_100k"
 
 
@@ -255,6 +256,38 @@ class Runner:
                            max_seq_len=self.max_seq_len, variant=self.variant, math=self.math,
                            num_stages=self.stages, phase1_event=phase1_event,
                            ctas_per_sm=self.ctas_per_sm, fuse_partitions=self.fuse_partitions)
+
+    def check_status(self):
+        st = self.pa.pa_read_device_status(self.ws)
+        if st != self.pa.PA_OK:
+            raise RuntimeError(f"device status {st}: {self.pa.pa_status_string(st)}")
+
+
+class ChunkRunner:
+    """The same cache as a Runner, queried with chunks of `tokens` tokens per
+    sequence (pa_chunks_forward)."""
+
+    def __init__(self, case, device, tokens):
+        import paged_decode_attention_v2_gb300 as pa
+        self.pa = pa
+        self.case = case
+        q, qs = workloads.chunk_queries(case, tokens)
+        self.q = q.to(device)
+        self.q_start = qs.to(device)
+        self.kc = case.key_cache.to(device)
+        self.vc = case.value_cache.to(device)
+        self.bt = case.block_tables.to(device)
+        self.sl = case.seq_lens.to(device)
+        self.out = torch.empty_like(self.q)
+        self.tokens = tokens
+        self.ws = pa.alloc_workspace(self.q.shape[0], case.num_heads, case.head_size,
+                                     case.max_seq_len, case.partition_size, device=device)
+
+    def step(self, phase1_event=None, **_):
+        self.pa.pa_chunks_forward(self.out, self.q, self.kc, self.vc, self.bt, self.sl,
+                                  self.q_start, self.case.scale, self.case.partition_size,
+                                  self.ws, max_seq_len=self.case.max_seq_len,
+                                  max_chunk=self.tokens)
 
     def check_status(self):
         st = self.pa.pa_read_device_status(self.ws)
@@ -474,6 +507,22 @@ def run_ours(args):
             "variant": "v2" if r2.is_v2 else "v1",
             "phase1_ms": round(statistics.mean(p1), 5) if p1 else None}}
         del r2
+    if world == 1 and not args.no_secondary:
+        # query chunks (speculative-decoding verification shape): the headline
+        # cache with 4-token chunks per sequence
+        cr = ChunkRunner(case, device, CHUNK_TOKENS)
+        for _ in range(max(args.warmup, 3)):
+            cr.step()
+        msc, _ = time_steps(cr, min(args.steps, 500), flush)
+        cr.check_status()
+        mc = statistics.mean(msc)
+        line["chunks"] = {
+            "workload": f"{args.workload}, {CHUNK_TOKENS}-token query chunks",
+            "value": round(case.kv_bytes() / (mc / 1e3) / 1e9, 2), "unit": UNIT,
+            "frac_of_peak": round(case.kv_bytes() / (mc / 1e3) / 1e9 / peak, 4),
+            "ms_per_step": round(mc, 5),
+            "query_rows_per_s": round(cr.q.shape[0] / (mc / 1e3), 1)}
+        del cr
     if world == 1 and not args.no_cpu_baseline:
         sub, dt, nt = cpu_oracle_sample(case)
         line["cpu_baseline"] = {

@@ -493,11 +493,12 @@ struct SimtMath {
 
 // Register cap per thread: three CTAs of (NW + 1) warps must fit in one SM,
 // i.e. at most four warps' registers per SM sub-partition (16K registers).
-// (Groups of more than 8 heads keep twice the accumulators; they are left
-// uncapped rather than spill.)
+// Groups of more than 8 heads (and query chunks) keep twice the
+// accumulators: at 4 consumer warps they are capped at 200, so that two CTAs
+// fit (at 202 a second CTA did not); with fewer warps they are left uncapped.
 template <int NW, int GMAX>
 constexpr int kernel_max_regs() {
-  return GMAX > 8 ? 255 : (NW == 4 ? 128 : (NW == 2 ? 168 : 255));
+  return GMAX > 8 ? (NW == 4 ? 200 : 255) : (NW == 4 ? 128 : (NW == 2 ? 168 : 255));
 }
 
 // ---------------------------------------------------------------------------
@@ -787,10 +788,17 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) __maxnreg__((kernel_max_regs
           const uint32_t vdst = kdst + HALF_BYTES;
 #pragma unroll
           for (int pn = 0; pn < NPANELS; ++pn) {
-            tma_load_2d_hint(kdst + pn * geom.panel_bytes, &tmap_k, pn * (kPanelBytes / ELT), y,
-                             full0 + 8 * st, kv_policy);
-            tma_load_2d_hint(vdst + pn * geom.panel_bytes, &tmap_v, pn * (kPanelBytes / ELT), y,
-                             full0 + 8 * st, kv_policy);
+            if constexpr (Math::kChunk) {  // the next row group re-reads these pages: keep them
+              tma_load_2d(kdst + pn * geom.panel_bytes, &tmap_k, pn * (kPanelBytes / ELT), y,
+                          full0 + 8 * st);
+              tma_load_2d(vdst + pn * geom.panel_bytes, &tmap_v, pn * (kPanelBytes / ELT), y,
+                          full0 + 8 * st);
+            } else {
+              tma_load_2d_hint(kdst + pn * geom.panel_bytes, &tmap_k, pn * (kPanelBytes / ELT), y,
+                               full0 + 8 * st, kv_policy);
+              tma_load_2d_hint(vdst + pn * geom.panel_bytes, &tmap_v, pn * (kPanelBytes / ELT), y,
+                               full0 + 8 * st, kv_policy);
+            }
           }
         }
         if constexpr (Math::kChunk) {

@@ -183,6 +183,20 @@ DESCRIPTIONS = {
 }
 
 
+def chunk_queries(case: DecodeCase, tokens: int, seed: int = 7):
+    """Query chunks of `tokens` tokens for every sequence of a case (its last
+    tokens, so each sequence must hold at least that many): q [B * tokens, H,
+    D] drawn N(0, 1) and rounded to the case's dtype, and q_start [B + 1]."""
+    B, H, D = case.query.shape
+    if int(case.seq_lens.min()) < tokens:
+        raise ValueError("a sequence is shorter than its chunk")
+    g = torch.Generator(device="cpu")
+    g.manual_seed(SEED_BASE + 5000 + seed)
+    q = _round(torch.randn(B * tokens, H, D, generator=g), case.dtype)
+    q_start = torch.arange(0, B * tokens + 1, tokens, dtype=torch.int32)
+    return q, q_start
+
+
 def config_case(name: str, partition_size: int | None = None,
                 seed_offset: int = 0) -> DecodeCase:
     """One of the five named workloads, drawn from seed SEED_BASE + index
