@@ -494,11 +494,13 @@ struct SimtMath {
 // Register cap per thread: three CTAs of (NW + 1) warps must fit in one SM,
 // i.e. at most four warps' registers per SM sub-partition (16K registers).
 // Groups of more than 8 heads (and query chunks) keep twice the
-// accumulators: at 4 consumer warps they are capped at 200, so that two CTAs
-// fit (at 202 a second CTA did not); with fewer warps they are left uncapped.
+// accumulators: at 4 consumer warps they are capped at 168, so that two CTAs
+// (10 warps, three on some sub-partitions) fit: 3 x 168 x 32 <= 16K, while at
+// 192 only two warps fit per sub-partition and the SM holds one CTA.  With
+// fewer warps they are left uncapped.
 template <int NW, int GMAX>
 constexpr int kernel_max_regs() {
-  return GMAX > 8 ? (NW == 4 ? 200 : 255) : (NW == 4 ? 128 : (NW == 2 ? 168 : 255));
+  return GMAX > 8 ? (NW == 4 ? 168 : 255) : (NW == 4 ? 128 : (NW == 2 ? 168 : 255));
 }
 
 // ---------------------------------------------------------------------------
