@@ -270,6 +270,86 @@ int default_stages(size_t stage_bytes) {
   return n < 2 ? 2 : (n > 8 ? 8 : n);
 }
 
+// Phase 2 of one call: kernel, grid and parameters.  It is planned before
+// Phase 1 is enqueued, so that nothing can fail between the two launches.
+struct Phase2Plan {
+  ReduceParams r;
+  const void *fn = nullptr;
+  long long ctas = 0;
+};
+
+pa_status_t plan_phase2(const Call &c, const AttnParams &p, const DeviceFacts *dev,
+                        long long prows, Phase2Plan *out) {
+  memset(&out->r, 0, sizeof out->r);
+  out->r.out = c.out;
+  out->r.max_logits = p.max_logits;
+  out->r.exp_sums = p.exp_sums;
+  out->r.tmp_out = p.tmp_out;
+  out->r.seq_lens = c.seq_lens;
+  out->r.status = p.status;
+  out->r.num_seqs = query_rows(c);  // Phase 2 rows: (query row, head)
+  out->r.num_heads = c.num_heads;
+  out->r.head_size = c.head_size;
+  out->r.max_parts = p.max_parts;
+  out->r.partition_size = c.partition_size;
+  out->r.max_seq_len = c.max_seq_len;
+  out->r.fuse_limit = p.fuse_limit;
+  out->r.row_limit = p.row_limit;
+  // Team size W (warps per task) and column split: the pair that minimises
+  // the chain of the longest task (1 + its rounds of loads, a round being one
+  // batch of NB partitions per thread) plus 2 for every further wave of
+  // tasks (the typical task, with sequences of mixed lengths, takes one
+  // round).  Only max_seq_len is known here, so the longest task is sized
+  // from it.
+  int occ = 0;
+  {
+    const void *probe = reduce_kernel(c.dtype, 1);
+    pa_status_t so = occupancy(probe, 256, 0, &occ);
+    if (so != PA_OK) return so;
+    if (occ < 1) return PA_ERR_UNSUPPORTED;
+  }
+  const long long resident_warps = (long long)occ * dev->sm_count * 8;
+  int best_w = 1, best_ds = 1, best_vpt = 1;
+  long long best_cost = -1;
+  for (int w = 1; w <= 8; w *= 2) {
+    for (int ds = 1; c.head_size / 4 / ds >= 4; ds *= 2) {
+      const int f4 = c.head_size / 4 / ds;  // float4 columns per task
+      const int vpt = f4 > 32 ? f4 / 32 : 1;
+      if (vpt > 2) continue;
+      const int lanes = f4 / vpt;
+      const long long slots = (long long)w * (32 / lanes);
+      const long long nb = vpt == 1 ? 4 : 2;  // the kernel's batch (NB)
+      const long long rounds = (p.max_parts + slots * nb - 1) / (slots * nb);
+      const long long conc = resident_warps / w;
+      const long long waves = (prows * ds + conc - 1) / conc;
+      const long long cost = (1 + rounds) + 2 * (waves - 1);
+      if (best_cost < 0 || cost < best_cost) {
+        best_cost = cost;
+        best_w = w;
+        best_ds = ds;
+        best_vpt = vpt;
+      }
+    }
+  }
+  out->r.cols_per_cta = c.head_size / best_ds;
+  out->r.warps_per_head = best_w;
+  const void *rfn = reduce_kernel(c.dtype, best_vpt);
+  if (!rfn) return PA_ERR_UNSUPPORTED;
+  out->fn = rfn;
+  int occ_k = 0;
+  {
+    pa_status_t so = occupancy(rfn, 256, 0, &occ_k);
+    if (so != PA_OK) return so;
+    if (occ_k < 1) return PA_ERR_UNSUPPORTED;
+  }
+  // persistent: never more CTAs than are resident at once
+  const long long teams_per_cta = 8 / best_w;
+  long long ctas = (prows * best_ds + teams_per_cta - 1) / teams_per_cta;
+  if (ctas > (long long)occ_k * dev->sm_count) ctas = (long long)occ_k * dev->sm_count;
+  out->ctas = ctas;
+  return PA_OK;
+}
+
 pa_status_t launch(const Call &c, bool v2, const pa_options_t &opt) {
   DeviceFacts *dev = nullptr;
   pa_status_t st = device_facts(&dev);
@@ -366,6 +446,22 @@ pa_status_t launch(const Call &c, bool v2, const pa_options_t &opt) {
   p.scale_log2 = (float)((double)c.scale * 1.4426950408889634);
   p.wait_limit_ns = opt.wait_limit_ns ? opt.wait_limit_ns : kDefaultWaitLimitNs;
 
+  // Phase 2 runs unless there are no rows, or the combine is fused and covers
+  // every sequence (Phase 1 then also writes the empty ones' zeros).  When it
+  // runs, it returns Phase 1's work counter to zero after its wait, so that
+  // Phase 1's CTAs can retire without a last-CTA-out handshake.
+  const long long prows = (long long)query_rows(c) * c.num_heads;
+  const bool run_p2 =
+      v2 && prows > 0 &&
+      !(p.fuse_limit > 0 && max_parts_of(c.max_seq_len, c.partition_size) <= p.fuse_limit);
+  Phase2Plan plan;
+  if (run_p2) {
+    st = plan_phase2(c, p, dev, prows, &plan);
+    if (st != PA_OK) return st;
+    plan.r.sched = p.sched;
+    p.sched_reset_later = 1;
+  }
+
   st = ensure_smem(k.fn, smem);
   if (st != PA_OK) return st;
 
@@ -400,88 +496,18 @@ pa_status_t launch(const Call &c, bool v2, const pa_options_t &opt) {
     cudaError_t e = cudaLaunchKernelExC(&cfg, k.fn, args);
     if (e != cudaSuccess) return fail_cuda("launch attention kernel", e);
   }
-  if (!v2) return PA_OK;
-  // With the combine fused, Phase 2 has work only for sequences of more than
-  // fuse_limit partitions (Phase 1 then also wrote the empty ones' zeros).
-  if (p.fuse_limit > 0 && max_parts_of(c.max_seq_len, c.partition_size) <= p.fuse_limit)
-    return PA_OK;
+  if (!run_p2) return PA_OK;
+
   if (opt.phase1_event) {
     cudaError_t e = cudaEventRecord(static_cast<cudaEvent_t>(opt.phase1_event), c.stream);
-    if (e != cudaSuccess) return fail_cuda("cudaEventRecord(phase1_event)", e);
-  }
-
-  // ---- Phase 2 (chained with programmatic dependent launch)
-  ReduceParams r;
-  memset(&r, 0, sizeof r);
-  r.out = c.out;
-  r.max_logits = p.max_logits;
-  r.exp_sums = p.exp_sums;
-  r.tmp_out = p.tmp_out;
-  r.seq_lens = c.seq_lens;
-  r.status = p.status;
-  r.num_seqs = query_rows(c);  // Phase 2 rows: (query row, head)
-  r.num_heads = c.num_heads;
-  r.head_size = c.head_size;
-  r.max_parts = p.max_parts;
-  r.partition_size = c.partition_size;
-  r.max_seq_len = c.max_seq_len;
-  r.fuse_limit = p.fuse_limit;
-  r.row_limit = p.row_limit;
-  // Team size W (warps per task) and column split: the pair that minimises
-  // the chain of the longest task (1 + its rounds of loads, a round being one
-  // batch of NB partitions per thread) plus 2 for every further wave of
-  // tasks (the typical task, with sequences of mixed lengths, takes one
-  // round).  Only max_seq_len is known here, so the longest task is sized
-  // from it.
-  const long long prows = (long long)query_rows(c) * c.num_heads;
-  if (prows == 0) return PA_OK;
-  int occ = 0;
-  {
-    const void *probe = reduce_kernel(c.dtype, 1);
-    pa_status_t so = occupancy(probe, 256, 0, &occ);
-    if (so != PA_OK) return so;
-    if (occ < 1) return PA_ERR_UNSUPPORTED;
-  }
-  const long long resident_warps = (long long)occ * dev->sm_count * 8;
-  int best_w = 1, best_ds = 1, best_vpt = 1;
-  long long best_cost = -1;
-  for (int w = 1; w <= 8; w *= 2) {
-    for (int ds = 1; c.head_size / 4 / ds >= 4; ds *= 2) {
-      const int f4 = c.head_size / 4 / ds;  // float4 columns per task
-      const int vpt = f4 > 32 ? f4 / 32 : 1;
-      if (vpt > 2) continue;
-      const int lanes = f4 / vpt;
-      const long long slots = (long long)w * (32 / lanes);
-      const long long nb = vpt == 1 ? 4 : 2;  // the kernel's batch (NB)
-      const long long rounds = (p.max_parts + slots * nb - 1) / (slots * nb);
-      const long long conc = resident_warps / w;
-      const long long waves = (prows * ds + conc - 1) / conc;
-      const long long cost = (1 + rounds) + 2 * (waves - 1);
-      if (best_cost < 0 || cost < best_cost) {
-        best_cost = cost;
-        best_w = w;
-        best_ds = ds;
-        best_vpt = vpt;
-      }
+    if (e != cudaSuccess) {
+      cudaMemsetAsync(p.sched, 0, 2 * sizeof(int), c.stream);  // Phase 2 will not reset it
+      return fail_cuda("cudaEventRecord(phase1_event)", e);
     }
   }
-  r.cols_per_cta = c.head_size / best_ds;
-  r.warps_per_head = best_w;
-  const void *rfn = reduce_kernel(c.dtype, best_vpt);
-  if (!rfn) return PA_ERR_UNSUPPORTED;
-  int occ_k = 0;
-  {
-    pa_status_t so = occupancy(rfn, 256, 0, &occ_k);
-    if (so != PA_OK) return so;
-    if (occ_k < 1) return PA_ERR_UNSUPPORTED;
-  }
-  // persistent: never more CTAs than are resident at once
-  const long long teams_per_cta = 8 / best_w;
-  long long ctas = (prows * best_ds + teams_per_cta - 1) / teams_per_cta;
-  if (ctas > (long long)occ_k * dev->sm_count) ctas = (long long)occ_k * dev->sm_count;
   cudaLaunchConfig_t cfg;
   memset(&cfg, 0, sizeof cfg);
-  cfg.gridDim = dim3((unsigned)ctas, 1, 1);
+  cfg.gridDim = dim3((unsigned)plan.ctas, 1, 1);
   cfg.blockDim = dim3(256, 1, 1);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = c.stream;
@@ -490,9 +516,12 @@ pa_status_t launch(const Call &c, bool v2, const pa_options_t &opt) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  void *rargs[1] = {&r};
-  cudaError_t e = cudaLaunchKernelExC(&cfg, rfn, rargs);
-  if (e != cudaSuccess) return fail_cuda("launch reduce kernel", e);
+  void *rargs[1] = {&plan.r};
+  cudaError_t e = cudaLaunchKernelExC(&cfg, plan.fn, rargs);
+  if (e != cudaSuccess) {
+    cudaMemsetAsync(p.sched, 0, 2 * sizeof(int), c.stream);  // see above
+    return fail_cuda("launch reduce kernel", e);
+  }
   return PA_OK;
 }
 

@@ -573,6 +573,20 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) __maxnreg__((kernel_max_regs
     if (lane == 0) {
       prefetch_tmap(&tmap_k);
       prefetch_tmap(&tmap_v);
+      // The block-table entries of a CTA's first item are read right after
+      // seq_lens (which locates the item): fetch them into L2 meanwhile, so
+      // that the first K/V copy waits one DRAM round trip less.  V1: the
+      // item's sequence is blockIdx / Hkv.  V2: the first items of all CTAs
+      // lie at the head of the table, so CTA b fetches its b-th 128-byte line.
+      const char *bt0 = reinterpret_cast<const char *>(p.block_tables);
+      if (!p.write_partials && !Math::kChunk) {
+        const int s0 = (int)blockIdx.x / p.num_kv_heads;
+        if (s0 < p.num_seqs && p.max_blocks_per_seq > 0)
+          prefetch_l2(bt0 + (size_t)s0 * p.max_blocks_per_seq * sizeof(int32_t));
+      } else {
+        const size_t bytes = (size_t)p.num_seqs * p.max_blocks_per_seq * sizeof(int32_t);
+        if ((size_t)blockIdx.x * 128 < bytes) prefetch_l2(bt0 + (size_t)blockIdx.x * 128);
+      }
     }
     const int U = p.unit_rows;
     const int units_per_stage = ST / U;
@@ -1047,13 +1061,18 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) __maxnreg__((kernel_max_regs
     pdl_launch_dependents();
   }
 
-  // ---- the last CTA out resets the work counter for the next launch
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    __threadfence();
-    if (atomicAdd(p.sched + 1, 1) == (int)gridDim.x - 1) {
-      atomicExch(p.sched, 0);
-      atomicExch(p.sched + 1, 0);
+  // ---- the work counter goes back to zero for the next launch: in the
+  // Phase 2 kernel after its wait, else here, by the last CTA out (a fence
+  // and an atomic round trip at the end of every CTA, which the Phase 2 reset
+  // takes off the critical path)
+  if (!p.sched_reset_later) {
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      __threadfence();
+      if (atomicAdd(p.sched + 1, 1) == (int)gridDim.x - 1) {
+        atomicExch(p.sched, 0);
+        atomicExch(p.sched + 1, 0);
+      }
     }
   }
 }

@@ -24,7 +24,9 @@ struct AttnParams {
   float *exp_sums;             // [B][H][max_parts]   (V2)
   float *tmp_out;              // [B][H][max_parts][D] (V2)
   int *status;                 // workspace status word
-  int *sched;                  // [0] next work item, [1] CTAs finished (reset by the last)
+  int *sched;                  // [0] next work item, [1] CTAs finished
+  int sched_reset_later;       // 1: the Phase 2 launch that follows zeroes sched;
+                               // 0: the last CTA out does
   int num_seqs, num_heads, num_kv_heads, group;  // group = H / Hkv
   int block_size, log2_block_size;
   int unit_rows, log2_unit_rows;  // rows per TMA box: min(block_size, stage tokens)
@@ -62,6 +64,7 @@ struct ReduceParams {
                         // sequence's length, rows being sequences)
   int cols_per_cta;    // columns of one task: head_size / (column split)
   int warps_per_head;  // warps of the team that serves one task: 1, 2, 4 or 8
+  int *sched;          // non-null: Phase 1's work counters, zeroed after the wait
 };
 
 enum MathKind { kMathSimt = 1, kMathTensor = 2 };

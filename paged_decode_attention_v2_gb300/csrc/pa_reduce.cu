@@ -92,6 +92,11 @@ __global__ void __launch_bounds__(kReduceThreads, 4)
   // (in chunk mode the counts are Phase 1 results: read after the wait)
   int np_next = task < ntasks && !p.row_limit ? partitions_of(p, task / dsplit) : 0;
   pdl_wait_primary();
+  // Phase 1 has completed: its work counters go back to zero for the next call
+  if (p.sched && blockIdx.x == 0 && threadIdx.x == 0) {
+    p.sched[0] = 0;
+    p.sched[1] = 0;
+  }
   if (p.row_limit && task < ntasks) np_next = partitions_of(p, task / dsplit);
   pdl_launch_dependents();  // the next kernel still waits for this grid to complete
 

@@ -126,6 +126,24 @@ def test_fused_combine_reads_every_partition():
                      "fused combine")
 
 
+@pytest.mark.parametrize("variant,fuse", [(pa.PA_VARIANT_V1, 0), (pa.PA_VARIANT_V2, 0),
+                                          (pa.PA_VARIANT_V2, 1), (pa.PA_VARIANT_V2, 16)])
+def test_work_counters_return_to_zero(variant, fuse):
+    """After every call the work-queue counters (words 1 and 2 of the status
+    block) are zero again, whoever resets them: Phase 1's last CTA (V1, or V2
+    with every sequence combined inside Phase 1) or the Phase 2 kernel after
+    its wait.  Repeated calls give the oracle's result each time."""
+    case = workloads.make_case("counters", 12, 3, 16, 2, 128, torch.bfloat16, 16, [5, 300, 1100],
+                               partition_size=256, extra_blocks=2)
+    ref = reference(case)
+    dc = DeviceCase(case)
+    for _ in range(3):
+        assert_close(dc.run(variant=variant, fuse_partitions=fuse), ref, torch.bfloat16,
+                     f"variant {variant}, fuse {fuse}")
+        words = dc.ws[:12].view(torch.int32).cpu().tolist()
+        assert words == [0, 0, 0], words
+
+
 @pytest.mark.parametrize("fuse", [16, 0])
 @pytest.mark.parametrize("dtype,H,Hkv,D", [(torch.float32, 4, 1, 64), (torch.bfloat16, 16, 2, 128)])
 def test_writes_stay_inside_out_and_workspace(dtype, H, Hkv, D, fuse):
