@@ -261,14 +261,7 @@ AttnKernelInfo pick_kernel(int math, int dtype, int head_size, int group) {
   return AttnKernelInfo{nullptr, 0, 0, 0};
 }
 
-// Default pipeline depth: about 64 KB of K+V stages per CTA.  Measured on
-// GB300, three CTAs per SM with two 32 KB stages each stream faster than
-// fewer CTAs with deeper rings: the other CTAs on the SM cover each CTA's
-// start-up and epilogue.
-int default_stages(size_t stage_bytes) {
-  int n = (int)((64 * 1024) / stage_bytes);
-  return n < 2 ? 2 : (n > 8 ? 8 : n);
-}
+
 
 // Phase 2 of one call: kernel, grid and parameters.  It is planned before
 // Phase 1 is enqueued, so that nothing can fail between the two launches.
@@ -370,14 +363,34 @@ pa_status_t launch(const Call &c, bool v2, const pa_options_t &opt) {
 
   const int elt = elt_size(c.dtype);
   const size_t stage_bytes = (size_t)k.stage_tokens * c.head_size * elt * 2;
-  int stages = opt.num_stages > 0 ? opt.num_stages : default_stages(stage_bytes);
-  if (stages < 2 || stages > 16) return PA_ERR_INVALID_ARG;
   const bool simt = math == kMathSimt;
-  size_t smem = attn_smem_bytes(c.head_size, elt, k.consumer_warps, k.max_group, stages, simt);
-  while (smem > (size_t)dev->max_smem_optin && stages > 2 && opt.num_stages <= 0) {
-    --stages;
-    smem = attn_smem_bytes(c.head_size, elt, k.consumer_warps, k.max_group, stages, simt);
+  const int threads = (k.consumer_warps + 1) * 32;
+  // Pipeline depth: the number of stages that keeps the most K/V bytes in
+  // flight per SM (resident CTAs x stages x stage bytes); on a tie the
+  // shallower ring, whose extra CTAs cover one another's start-up and
+  // epilogue (measured on GB300: three CTAs of two 32 KB stages stream faster
+  // than two CTAs of three).
+  int stages = opt.num_stages > 0 ? opt.num_stages : 0;
+  if (stages > 0 && (stages < 2 || stages > 16)) return PA_ERR_INVALID_ARG;
+  if (stages == 0) {
+    long long best = 0;
+    for (int n = 2; n <= 8; ++n) {
+      const size_t b = attn_smem_bytes(c.head_size, elt, k.consumer_warps, k.max_group, n, simt);
+      if (b > (size_t)dev->max_smem_optin) break;
+      st = ensure_smem(k.fn, b);
+      if (st != PA_OK) return st;
+      int fit = 0;
+      st = occupancy(k.fn, threads, b, &fit);
+      if (st != PA_OK) return st;
+      const long long flight = (long long)fit * n * (long long)stage_bytes;
+      if (flight > best) {
+        best = flight;
+        stages = n;
+      }
+    }
+    if (stages <= 0) return PA_ERR_UNSUPPORTED;
   }
+  size_t smem = attn_smem_bytes(c.head_size, elt, k.consumer_warps, k.max_group, stages, simt);
   if (smem > (size_t)dev->max_smem_optin) return PA_ERR_UNSUPPORTED;
 
   const int unit_rows = c.block_size < k.stage_tokens ? c.block_size : k.stage_tokens;
@@ -467,7 +480,6 @@ pa_status_t launch(const Call &c, bool v2, const pa_options_t &opt) {
 
   // Persistent grid: as many CTAs as fit on the GPU (or the requested number
   // per SM), never more than there can be work items.
-  const int threads = (k.consumer_warps + 1) * 32;
   int per_sm = 0;
   st = occupancy(k.fn, threads, smem, &per_sm);
   if (st != PA_OK) return st;

@@ -514,15 +514,19 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) __maxnreg__((kernel_max_regs
   constexpr int NPANELS = ROW_BYTES / kPanelBytes;
   constexpr int HALF_BYTES = ST * ROW_BYTES;  // K (or V) bytes of one stage
   constexpr int NCONS = NW * 32;
-  constexpr int QBYTES = GMAX * D * ELT;      // query slot of one stage
-  // The consumer warps merge their states in the K/V bytes of an item's last
-  // stage when they fit (the data is dead by then; the slot is released after
-  // the merge), else in a dedicated area.
+  constexpr int QBYTES = GMAX * D * ELT;      // queries of one item
+  // A stage is its K and V bytes followed by its query slot (padded to keep
+  // the next stage's TMA destinations 1024-byte aligned for the 128B swizzle).
+  constexpr int QSLOT = (QBYTES + 1023) & ~1023;
+  constexpr int STAGE_BYTES = 2 * HALF_BYTES + QSLOT;
+  // The consumer warps merge their states in an item's last stage (K, V and
+  // query bytes, dead by then: the queries were taken into registers or the
+  // fp32 table when the item began); the stage goes back to the producer
+  // after the merge.
   constexpr int MERGE_BYTES_STATE = NW * GMAX * (D + 4) * 4 + NW * GMAX * 2 * 4;
   constexpr int MERGE_BYTES_FUSE = (3 * GMAX * kFuseCap + 4) * 4;  // fused combine scratch
-  constexpr int MERGE_BYTES =
-      MERGE_BYTES_STATE > MERGE_BYTES_FUSE ? MERGE_BYTES_STATE : MERGE_BYTES_FUSE;
-  constexpr bool MERGE_IN_SLOT = MERGE_BYTES <= 2 * HALF_BYTES;
+  static_assert(MERGE_BYTES_STATE <= STAGE_BYTES && MERGE_BYTES_FUSE <= STAGE_BYTES,
+                "the merge fits in one stage");
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int NST = p.num_stages;
@@ -531,18 +535,14 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) __maxnreg__((kernel_max_regs
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t *ring = smem;
-  uint8_t *qbuf = ring + (size_t)NST * 2 * HALF_BYTES;
-  uint8_t *merge_area = qbuf + (size_t)NST * QBYTES;
-  StageInfo *info =
-      reinterpret_cast<StageInfo *>(merge_area + (MERGE_IN_SLOT ? 0 : MERGE_BYTES));
+  uint8_t *ring = smem;  // NST x [K | V | queries]
+  StageInfo *info = reinterpret_cast<StageInfo *>(ring + (size_t)NST * STAGE_BYTES);
   uint64_t *bars = reinterpret_cast<uint64_t *>(info + NST);
   volatile int *flags = reinterpret_cast<volatile int *>(bars + 2 * NST + 2);
   float *simt_q = reinterpret_cast<float *>(
       (reinterpret_cast<uintptr_t>(flags) + 16 + 15) & ~uintptr_t(15));
   float *simt_p = simt_q + GMAX * (D + 8);
   const uint32_t ring_u32 = smem_u32(ring);
-  const uint32_t qbuf_u32 = smem_u32(qbuf);
   const uint32_t full0 = smem_u32(bars), empty0 = full0 + 8 * NST, never = full0 + 16 * NST;
   const uint32_t cons_bar = never + 8;  // consumer-warp barrier (bounded waits)
 
@@ -800,7 +800,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) __maxnreg__((kernel_max_regs
         }
         __syncwarp();
         if (y >= 0) {
-          const uint32_t kdst = ring_u32 + (uint32_t)st * 2 * HALF_BYTES + (uint32_t)lane * geom.unit_bytes;
+          const uint32_t kdst = ring_u32 + (uint32_t)st * STAGE_BYTES + (uint32_t)lane * geom.unit_bytes;
           const uint32_t vdst = kdst + HALF_BYTES;
 #pragma unroll
           for (int pn = 0; pn < NPANELS; ++pn) {
@@ -821,13 +821,14 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) __maxnreg__((kernel_max_regs
           if (first && lane < ntok) {  // one copy per token: its G heads are contiguous
             const T *q = static_cast<const T *>(p.query) +
                          ((size_t)(row0 + lane) * p.num_heads + (size_t)kvh * p.group) * D;
-            bulk_load(qbuf_u32 + (uint32_t)st * QBYTES + (uint32_t)(lane * qbytes), q,
+            bulk_load(ring_u32 + (uint32_t)st * STAGE_BYTES + 2 * HALF_BYTES + (uint32_t)(lane * qbytes), q,
                       (uint32_t)qbytes, full0 + 8 * st);
           }
         } else if (first && lane == 0) {
           const T *q = static_cast<const T *>(p.query) +
                        ((size_t)s * p.num_heads + (size_t)kvh * p.group) * D;
-          bulk_load(qbuf_u32 + (uint32_t)st * QBYTES, q, (uint32_t)qbytes, full0 + 8 * st);
+          bulk_load(ring_u32 + (uint32_t)st * STAGE_BYTES + 2 * HALF_BYTES, q, (uint32_t)qbytes,
+                    full0 + 8 * st);
         }
         ++i;
         const int next_rel = ((stage_tok0 + ST) >> p.log2_block_size) - win0;
@@ -893,9 +894,10 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) __maxnreg__((kernel_max_regs
       if (h.flags & kStageEnd) break;
       if (h.flags & kStageFirst) {
         if constexpr (Math::kChunk)  // rows = (token, head) pairs; h.pad = first token's key limit
-          math.begin_item(qbuf + (size_t)st * QBYTES, h.np, lane, NCONS, h.pad, p.group);
+          math.begin_item(ring + (size_t)st * STAGE_BYTES + 2 * HALF_BYTES, h.np, lane, NCONS,
+                          h.pad, p.group);
         else
-          math.begin_item(qbuf + (size_t)st * QBYTES, p.group, lane, NCONS);
+          math.begin_item(ring + (size_t)st * STAGE_BYTES + 2 * HALF_BYTES, p.group, lane, NCONS);
         if constexpr (SIMT) {
           ok = cons_sync();  // the shared fp32 query table is complete
           if (!ok) break;
@@ -904,7 +906,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) __maxnreg__((kernel_max_regs
       const int tile_tok0 = h.tok0 + warp * kTileTokens;
       const int valid = max(0, min(kTileTokens, h.tok_end - tile_tok0));
       if (valid > 0) {
-        const uint32_t kbase = ring_u32 + (uint32_t)st * 2 * HALF_BYTES;
+        const uint32_t kbase = ring_u32 + (uint32_t)st * STAGE_BYTES;
         math.tile(kbase, kbase + HALF_BYTES, geom, warp * kTileTokens, valid, lane, p.scale_log2,
                   tile_tok0);
       }
@@ -915,7 +917,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) __maxnreg__((kernel_max_regs
       }
 
       // ---- item done: merge the consumer warps' states (log-sum-exp), write
-      uint8_t *mb = MERGE_IN_SLOT ? ring + (size_t)st * 2 * HALF_BYTES : merge_area;
+      uint8_t *mb = ring + (size_t)st * STAGE_BYTES;
       float *m_s = reinterpret_cast<float *>(mb);
       float *l_s = m_s + NW * GMAX;
       float *o_s = l_s + NW * GMAX;
@@ -1042,8 +1044,8 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) __maxnreg__((kernel_max_regs
           if (threadIdx.x == 0) *cnt = 0;  // ready for the next launch
         }
       }
-      if (MERGE_IN_SLOT) {
-        // hand the slot back to the producer; its next TMA writes come after
+      {
+        // hand the stage back to the producer; its next TMA writes come after
         // our generic-proxy writes
         fence_proxy_async_smem();
         ok = cons_sync();

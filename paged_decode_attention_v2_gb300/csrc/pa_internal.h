@@ -78,18 +78,15 @@ struct AttnKernelInfo {
 };
 
 // Dynamic shared memory the attention kernel needs for `stages` stages (the
-// kernel's carve-up, in order: ring, query slots, merge area, stage headers,
-// mbarriers, flags, CUDA-core tables).
+// kernel's carve-up, in order: the ring of stages, each its K and V bytes and
+// a query slot padded to 1024 bytes; stage headers; mbarriers; flags;
+// CUDA-core tables).  The consumer warps merge inside an item's last stage, so
+// the merge takes no bytes of its own.
 inline size_t attn_smem_bytes(int head_size, int elt, int consumer_warps, int max_group,
                               int stages, bool simt) {
-  size_t stage = (size_t)consumer_warps * kTileTokens * head_size * elt * 2;
-  size_t ring = stage * stages;
-  size_t qslots = (size_t)max_group * head_size * elt * stages;
-  size_t merge = (size_t)consumer_warps * max_group * (head_size + 4) * 4 +
-                 (size_t)consumer_warps * max_group * 2 * 4;
-  const size_t fuse_scratch = (3 * (size_t)max_group * kFuseLimitMax + 4) * 4;
-  if (merge < fuse_scratch) merge = fuse_scratch;
-  if (merge <= stage) merge = 0;  // merged inside the item's last stage
+  const size_t kv = (size_t)consumer_warps * kTileTokens * head_size * elt * 2;
+  const size_t qslot = ((size_t)max_group * head_size * elt + 1023) & ~(size_t)1023;
+  size_t ring = (kv + qslot) * stages;
   size_t headers = 32 * (size_t)stages;
   size_t bars = 8 * (2 * (size_t)stages + 2);  // full, empty, never-set, consumer barrier
   size_t flags = 16 + 16;                      // flags + alignment
@@ -98,7 +95,7 @@ inline size_t attn_smem_bytes(int head_size, int elt, int consumer_warps, int ma
     simt_extra = (size_t)max_group * (head_size + 8) * 4 +               // q (fp32)
                  (size_t)consumer_warps * kTileTokens * max_group * 4;  // p tiles
   }
-  return 1024 /* alignment slack */ + ring + qslots + merge + headers + bars + flags + simt_extra;
+  return 1024 /* alignment slack */ + ring + headers + bars + flags + simt_extra;
 }
 
 // Kernel tables, one per translation unit (see pa_attn_*.cu).
