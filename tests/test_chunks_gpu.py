@@ -103,3 +103,22 @@ def test_chunks_refuse_f32():
                              c.block_tables.cuda(), c.seq_lens.cuda(), qs.cuda(), c.scale, 256,
                              ws, max_seq_len=c.max_seq_len, max_chunk=3)
     assert e.value.status == pa.PA_ERR_UNSUPPORTED
+
+
+def test_bench_chunk_workload_full_size():
+    """The benchmark's query-chunk step at full size: the c4_batch256 cache
+    (256 sequences, 32 q / 4 kv heads, D 128, bf16) with a 4-token chunk per
+    sequence from the workload generator, every output against the oracle."""
+    c = workloads.config_case("c4_batch256")
+    q, qs = workloads.chunk_queries(c, 4)
+    ref = oracle.query_chunks(q, c.key_cache, c.value_cache, c.block_tables, c.seq_lens, qs,
+                              c.scale)
+    dev = "cuda"
+    R, H, D = q.shape
+    ws = pa.alloc_workspace(R, H, D, c.max_seq_len, c.partition_size)
+    out = torch.full((R, H, D), float("nan"), dtype=c.dtype, device=dev)
+    pa.pa_chunks_forward(out, q.to(dev), c.key_cache.to(dev), c.value_cache.to(dev),
+                         c.block_tables.to(dev), c.seq_lens.to(dev), qs.to(dev), c.scale,
+                         c.partition_size, ws, max_seq_len=c.max_seq_len, max_chunk=4)
+    assert pa.pa_read_device_status(ws) == pa.PA_OK
+    assert_close(out, ref, c.dtype, "c4 cache, 4-token chunks")

@@ -33,6 +33,20 @@ def test_config_parity(name, P, variant):
     assert_close(out, ref, dc.case.dtype, f"{name} P={dc.case.partition_size} v{variant}")
 
 
+def test_gqa16_full_size_parity():
+    """Groups of 16 query heads (the 16-row kernel, two CTAs per SM of three
+    stages) at full size: c4_batch256's lengths and cache shape with 32 q / 2
+    kv heads, every output against the oracle, V2 and auto."""
+    c = dict(workloads.CONFIGS["c4_batch256"])
+    c.pop("index")
+    c["num_kv_heads"] = 2
+    case = workloads.make_case("gqa16", workloads.SEED_BASE + 77, **c)
+    ref = reference(case)
+    dc = DeviceCase(case)
+    for variant in (pa.PA_VARIANT_V2, pa.PA_VARIANT_AUTO):
+        assert_close(dc.run(variant=variant), ref, case.dtype, f"G=16 v{variant}")
+
+
 @pytest.mark.parametrize("name", ["c2_gqa_batch8", "c5_mixed_d256"])
 def test_config_parity_simt_math(name):
     """The CUDA-core path on 16-bit inputs (forced) meets the same bar."""
