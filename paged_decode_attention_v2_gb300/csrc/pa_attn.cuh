@@ -269,8 +269,10 @@ struct TensorMath {
   // Step 2: with every warp's stats in m_s/l_s [NW][GMAX], scale this warp's
   // O by exp2(m_w - M) / L (log-sum-exp weight and final normaliser) and
   // store it to o_w [GMAX][D+4]; the sum over warps is then the output.
+  // row_ml (one warp passes it): the merged (M, L) of every row, for the
+  // partials.
   __device__ __forceinline__ void store_scaled(float *o_w, const float *m_s, const float *l_s,
-                                               int nw, int lane) {
+                                               int nw, int lane, float2 *row_ml) {
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       float f[2];
@@ -281,6 +283,7 @@ struct TensorMath {
         for (int w = 0; w < nw; ++w) M = fmaxf(M, m_s[w * GMAX + h]);
         float L = 0.f;
         for (int w = 0; w < nw; ++w) L += l_s[w * GMAX + h] * exp2f(m_s[w * GMAX + h] - M);
+        if (row_ml && lane < 4) row_ml[h] = make_float2(M, L);
         f[j] = exp2f(m[nt][j] - M) / L;  // 0 for a warp that saw no token
         if constexpr (CHUNK) {
           if (!(L > 0.f)) f[j] = 0.f;  // a column that saw no key at all: zeros
@@ -477,13 +480,14 @@ struct SimtMath {
   }
 
   __device__ __forceinline__ void store_scaled(float *o_w, const float *m_s, const float *l_s,
-                                               int nw, int lane) {
+                                               int nw, int lane, float2 *row_ml) {
 #pragma unroll
     for (int gg = 0; gg < GMAX; ++gg) {
       float M = -CUDART_INF_F;
       for (int w = 0; w < nw; ++w) M = fmaxf(M, m_s[w * GMAX + gg]);
       float L = 0.f;
       for (int w = 0; w < nw; ++w) L += l_s[w * GMAX + gg] * exp2f(m_s[w * GMAX + gg] - M);
+      if (row_ml && lane == 0) row_ml[gg] = make_float2(M, L);
       const float f = exp2f(m[gg] - M) / L;
 #pragma unroll
       for (int j = 0; j < DPL; ++j) o_w[gg * (D + 4) + lane * DPL + j] = acc[gg][j] * f;
@@ -523,7 +527,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) __maxnreg__((kernel_max_regs
   // query bytes, dead by then: the queries were taken into registers or the
   // fp32 table when the item began); the stage goes back to the producer
   // after the merge.
-  constexpr int MERGE_BYTES_STATE = NW * GMAX * (D + 4) * 4 + NW * GMAX * 2 * 4;
+  constexpr int MERGE_BYTES_STATE = NW * GMAX * (D + 4) * 4 + NW * GMAX * 2 * 4 + GMAX * 8;
   constexpr int MERGE_BYTES_FUSE = (3 * GMAX * kFuseCap + 4) * 4;  // fused combine scratch
   static_assert(MERGE_BYTES_STATE <= STAGE_BYTES && MERGE_BYTES_FUSE <= STAGE_BYTES,
                 "the merge fits in one stage");
@@ -926,7 +930,10 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) __maxnreg__((kernel_max_regs
       math.stats(m_s + warp * GMAX, l_s + warp * GMAX, lane);
       ok = cons_sync();
       if (!ok) break;
-      math.store_scaled(o_s + (size_t)warp * GMAX * (D + 4), m_s, l_s, NW, lane);
+      // warp 0 also records each row's merged (M, L) for the partials
+      float2 *row_ml = reinterpret_cast<float2 *>(o_s + (size_t)NW * GMAX * (D + 4));
+      math.store_scaled(o_s + (size_t)warp * GMAX * (D + 4), m_s, l_s, NW, lane,
+                        warp == 0 ? row_ml : nullptr);
       ok = cons_sync();
       if (!ok) break;
       // out[h][d] = sum over warps of the scaled partial outputs (16 bytes a thread)
@@ -954,14 +961,9 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) __maxnreg__((kernel_max_regs
           const size_t row = orow * p.max_parts + h.part;
           *reinterpret_cast<float4 *>(p.tmp_out + row * D + d) = acc;
           if (d == 0) {
-            float M = -CUDART_INF_F;
-#pragma unroll
-            for (int w2 = 0; w2 < NW; ++w2) M = fmaxf(M, m_s[w2 * GMAX + hh]);
-            float L = 0.f;
-#pragma unroll
-            for (int w2 = 0; w2 < NW; ++w2) L += l_s[w2 * GMAX + hh] * exp2f(m_s[w2 * GMAX + hh] - M);
-            p.max_logits[row] = M * 0.69314718055994530942f;  // back to natural-log units
-            p.exp_sums[row] = L;
+            const float2 ml = row_ml[hh];
+            p.max_logits[row] = ml.x * 0.69314718055994530942f;  // back to natural-log units
+            p.exp_sums[row] = ml.y;
           }
         } else {
           T *o = static_cast<T *>(p.out) + orow * D + d;
