@@ -25,8 +25,9 @@
 //                  same log-sum-exp combine as Phase 2) and write either the
 //                  final output (V1) or the partition's max_logits /
 //                  exp_sums / normalised tmp_output (V2 Phase 1).
-// The last CTA to finish resets the work counter, so the next launch on
-// the workspace starts from zero.
+// The work counter goes back to zero for the next launch on the workspace:
+// the Phase 2 kernel resets it after its wait, else the last CTA to finish
+// does.
 //
 // Every wait is bounded (%globaltimer); a wait that runs out records
 // PA_ERR_DEVICE_TIMEOUT, the CTA lets its own in-flight copies land, and
@@ -1088,8 +1089,8 @@ AttnKernelInfo attn_info() {
 }
 
 // Consumer warps per CTA: a stage is NW x 16 tokens; keep it at 32 KB of K+V
-// for rows of 256 bytes or more (4, 2 or 1 warps), so that two stages leave
-// room for three CTAs on an SM.
+// for rows of 256 bytes or more (4, 2 or 1 warps), so that two stages (the
+// host's choice for up to 8 heads a group) leave room for three CTAs on an SM.
 template <typename T, int D>
 constexpr int consumer_warps() {
   return D * (int)sizeof(T) <= 256 ? 4 : (D * (int)sizeof(T) <= 512 ? 2 : 1);
