@@ -209,16 +209,21 @@ struct TensorMath {
       const float2 flo = MmaOp<T>::unpack(plo), fhi = MmaOp<T>::unpack(phi);
       l[nt][0] = l[nt][0] * al0 + (flo.x + fhi.x);
       l[nt][1] = l[nt][1] * al1 + (flo.y + fhi.y);
+      // no column of the n-tile raised its max: every factor is exp2(0) = 1
+      // and the rescale would change no bit
+      const bool same = mn0 == m[nt][0] && mn1 == m[nt][1];
       m[nt][0] = mn0;
       m[nt][1] = mn1;
       pb[nt][0] = movmatrix_trans(plo);
       pb[nt][1] = movmatrix_trans(phi);
+      if (!__all_sync(0xffffffffu, same)) {
 #pragma unroll
-      for (int mt = 0; mt < KS; ++mt) {
-        o[nt][mt][0] *= al0;
-        o[nt][mt][1] *= al1;
-        o[nt][mt][2] *= al0;
-        o[nt][mt][3] *= al1;
+        for (int mt = 0; mt < KS; ++mt) {
+          o[nt][mt][0] *= al0;
+          o[nt][mt][1] *= al1;
+          o[nt][mt][2] *= al0;
+          o[nt][mt][3] *= al1;
+        }
       }
     }
     // ---- rows past the end of the range hold stale or foreign data: zero
