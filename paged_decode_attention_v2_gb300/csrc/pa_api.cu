@@ -261,8 +261,6 @@ AttnKernelInfo pick_kernel(int math, int dtype, int head_size, int group) {
   return AttnKernelInfo{nullptr, 0, 0, 0};
 }
 
-
-
 // Phase 2 of one call: kernel, grid and parameters.  It is planned before
 // Phase 1 is enqueued, so that nothing can fail between the two launches.
 struct Phase2Plan {
@@ -273,21 +271,22 @@ struct Phase2Plan {
 
 pa_status_t plan_phase2(const Call &c, const AttnParams &p, const DeviceFacts *dev,
                         long long prows, Phase2Plan *out) {
-  memset(&out->r, 0, sizeof out->r);
-  out->r.out = c.out;
-  out->r.max_logits = p.max_logits;
-  out->r.exp_sums = p.exp_sums;
-  out->r.tmp_out = p.tmp_out;
-  out->r.seq_lens = c.seq_lens;
-  out->r.status = p.status;
-  out->r.num_seqs = query_rows(c);  // Phase 2 rows: (query row, head)
-  out->r.num_heads = c.num_heads;
-  out->r.head_size = c.head_size;
-  out->r.max_parts = p.max_parts;
-  out->r.partition_size = c.partition_size;
-  out->r.max_seq_len = c.max_seq_len;
-  out->r.fuse_limit = p.fuse_limit;
-  out->r.row_limit = p.row_limit;
+  ReduceParams &r = out->r;
+  memset(&r, 0, sizeof r);
+  r.out = c.out;
+  r.max_logits = p.max_logits;
+  r.exp_sums = p.exp_sums;
+  r.tmp_out = p.tmp_out;
+  r.seq_lens = c.seq_lens;
+  r.status = p.status;
+  r.num_seqs = query_rows(c);  // Phase 2 rows: (query row, head)
+  r.num_heads = c.num_heads;
+  r.head_size = c.head_size;
+  r.max_parts = p.max_parts;
+  r.partition_size = c.partition_size;
+  r.max_seq_len = c.max_seq_len;
+  r.fuse_limit = p.fuse_limit;
+  r.row_limit = p.row_limit;
   // Team size W (warps per task) and column split: the pair that minimises
   // the chain of the longest task (1 + its rounds of loads, a round being one
   // batch of NB partitions per thread) plus 2 for every further wave of
@@ -324,8 +323,8 @@ pa_status_t plan_phase2(const Call &c, const AttnParams &p, const DeviceFacts *d
       }
     }
   }
-  out->r.cols_per_cta = c.head_size / best_ds;
-  out->r.warps_per_head = best_w;
+  r.cols_per_cta = c.head_size / best_ds;
+  r.warps_per_head = best_w;
   const void *rfn = reduce_kernel(c.dtype, best_vpt);
   if (!rfn) return PA_ERR_UNSUPPORTED;
   out->fn = rfn;
