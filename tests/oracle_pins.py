@@ -292,6 +292,24 @@ def pin_empty_sequence(lib):
     assert np.array_equal(out[0], np.zeros_like(out[0]))
 
 
+def pin_attention_pairs_match_attention(lib):
+    """The (seq, head) pair entry point gives, for every pair in any order,
+    the row the whole-batch definition gives for that sequence and head:
+    the same arithmetic, so the same bits.  B = 5 and H = 4 differ, so a pair
+    decoded as (h, s) instead of (s, h) lands on another row (or out of the
+    batch), and the shuffled order catches an output written to the wrong
+    slot."""
+    c = small_case(22, B=5, H=4, Hkv=2, D=4, bs=4, lens=(3, 9, 1, 14, 6), k_mult=2.0)
+    ref = _run(lib, c)
+    pairs = [(s, h) for s in range(5) for h in range(4)]
+    order = np.random.default_rng(5).permutation(len(pairs))
+    pairs = [pairs[i] for i in order]
+    got = oracle.attention_pairs(pairs, c.query, c.key_cache, c.value_cache,
+                                 c.block_tables, c.seq_lens, c.scale, lib=lib)
+    for i, (s, h) in enumerate(pairs):
+        assert np.array_equal(got[i], ref[s, h]), ((s, h), got[i], ref[s, h])
+
+
 def _chunks_case(seed, lens, qlens, H=4, Hkv=2, D=4, bs=4, dtype=torch.float64):
     """A cache case plus query chunks: rows = sum(qlens) query vectors."""
     c = small_case(seed, B=len(lens), H=H, Hkv=Hkv, D=D, bs=bs, lens=lens, dtype=dtype)
@@ -352,7 +370,7 @@ ALL_PINS = [
     pin_zero_query_is_mean, pin_one_hot_logit, pin_linearity_in_v,
     pin_scale_folds_into_query, pin_gqa_head_map, pin_tail_masking,
     pin_pool_permutation, pin_partition_combine_equals_softmax,
-    pin_partials_closed_form, pin_empty_sequence,
+    pin_partials_closed_form, pin_empty_sequence, pin_attention_pairs_match_attention,
     pin_query_chunks_single_token_is_decode, pin_query_chunks_causal_brute_force,
     pin_query_chunks_first_token_sees_itself,
 ]

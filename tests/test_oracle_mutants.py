@@ -47,6 +47,8 @@ MUTANTS = [
     ("f16_exponent_bias", "e - 25); /* (1 + f/1024)", "e - 24); /* (1 + f/1024)"),
     ("f16_subnormal_scale", "ldexp((double)f, -24)", "ldexp((double)f, -25)"),
     ("bf16_wrong_half", "uint32_t u = (uint32_t)b << 16;", "uint32_t u = (uint32_t)b << 15;"),
+    ("pairs_s_h_swapped", "int s = pairs[2 * i], h = pairs[2 * i + 1];",
+     "int h = pairs[2 * i], s = pairs[2 * i + 1];"),
     ("dot_drops_last_dim", "for (int d = 0; d < D; ++d)\n    dot +=",
      "for (int d = 0; d < D - 1; ++d)\n    dot +="),
 ]
