@@ -667,7 +667,11 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) __maxnreg__((kernel_max_regs
       takers = per > 0 ? (c_total + per - 1) / per : 0;
       if ((int)blockIdx.x >= takers) item = c_total;  // past the last item: none
     }
-    auto grab_issue = [&]() -> int { return lane == 0 ? atomicAdd(p.sched, 1) : 0; };
+    // Predicated in PTX so that nothing consumes the result until the item
+    // ends: every CTA takes its first item at the same moment, and a select
+    // on the result (lane == 0 ? atomicAdd(..) : 0) would hold the producer
+    // for the whole round trip of atomics queued on one address.
+    auto grab_issue = [&]() -> int { return atomic_add_lane0(p.sched, lane); };
     auto grab_value = [&](int raw) -> int {
       return takers + __shfl_sync(0xffffffffu, raw, 0);
     };
@@ -851,6 +855,12 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) __maxnreg__((kernel_max_regs
       if (!ok) break;
       item = grab_value(next_raw);
     }
+    // Every copy of this CTA is issued: let the next kernel (Phase 2) be
+    // scheduled once every CTA has come this far.  Its CTAs then take the
+    // SMs that the first CTAs to finish leave free and sit in their own
+    // dependency wait, which still holds them until this grid has completed,
+    // instead of being launched only after the last CTA's epilogue.
+    pdl_launch_dependents();
     if (ok) {  // tell the consumers there is nothing more
       const int st = i % NST;
       if (i >= NST) {
@@ -1065,9 +1075,10 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) __maxnreg__((kernel_max_regs
       report(p.status, kStatusTimeout);
       flags[0] = 1;
     }
-    // Let the next kernel (Phase 2) be scheduled once every CTA is here; its
-    // own wait holds it until this grid has completed.  (Triggered earlier,
-    // its CTAs would crowd onto the few SMs that have room.)
+    // The producer normally triggered the next kernel already; this covers a
+    // producer that left early.  (Triggered at the start instead, Phase 2's
+    // CTAs would crowd onto the few SMs that have room while every CTA still
+    // streams.)
     pdl_launch_dependents();
   }
 

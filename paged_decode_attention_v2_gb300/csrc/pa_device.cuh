@@ -154,6 +154,19 @@ __device__ __forceinline__ int atomic_add_acq_rel_gpu(int *addr, int v) {
   return old;
 }
 
+// Lane 0 adds 1 to *addr and gets the old value; the other lanes get 0.  The
+// add is predicated, so the result register is read only where the caller
+// uses it, not at a select right after the issue.
+__device__ __forceinline__ int atomic_add_lane0(int *addr, int lane) {
+  int old = 0;
+  asm volatile(
+      "{\n .reg .pred p;\n setp.eq.s32 p, %1, 0;\n @p atom.global.add.s32 %0, [%2], 1;\n}"
+      : "+r"(old)
+      : "r"(lane), "l"(addr)
+      : "memory");
+  return old;
+}
+
 // Programmatic dependent launch: let the next kernel in the stream start its
 // prologue; it waits for this grid's completion before reading our results.
 __device__ __forceinline__ void pdl_launch_dependents() {

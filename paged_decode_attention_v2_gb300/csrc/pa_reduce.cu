@@ -13,8 +13,9 @@
 // "slots" take the partitions slot, slot + S, ... (S slots); each thread
 // issues the loads of up to NB of its partitions at once and folds them into
 // an online log-sum-exp state: running max m, running sum S = sum r_p e^-m
-// and the running weighted row.  The slots' states are merged with the same
-// rescale rule (shuffles inside a warp, shared memory across the team), so
+// and the running weighted row.  The slots' states are then merged with the
+// same rescale rule (shuffles inside a warp, shared memory across the team):
+// the common maximum first, then each state rescaled once and summed, so
 // the result is the formula above up to rounding.  The host sizes W and the
 // column split so that one batch covers the longest sequence's partitions.
 #include <math_constants.h>
@@ -31,23 +32,6 @@ struct LseAcc {
   float m, S;
   float4 a[VPT];
 };
-
-template <int VPT>
-__device__ __forceinline__ void lse_merge(LseAcc<VPT> &x, float m2, float S2,
-                                          const float4 (&a2)[VPT]) {
-  const float M = fmaxf(x.m, m2);
-  const float f1 = M == -CUDART_INF_F ? 0.f : expf(x.m - M);
-  const float f2 = M == -CUDART_INF_F ? 0.f : expf(m2 - M);
-  x.S = x.S * f1 + S2 * f2;
-#pragma unroll
-  for (int k = 0; k < VPT; ++k) {
-    x.a[k].x = x.a[k].x * f1 + a2[k].x * f2;
-    x.a[k].y = x.a[k].y * f1 + a2[k].y * f2;
-    x.a[k].z = x.a[k].z * f1 + a2[k].z * f2;
-    x.a[k].w = x.a[k].w * f1 + a2[k].w * f2;
-  }
-  x.m = M;
-}
 
 // Barrier of the W warps of team g (named barrier 1 + g; 0 is __syncthreads).
 __device__ __forceinline__ void team_sync(int g, int nthreads) {
@@ -160,21 +144,33 @@ __global__ void __launch_bounds__(kReduceThreads, 4)
       }
       acc.m = M;
     }
-    // merge the slots of the warp (lanes with the same column chunk)
-    for (int off = C; off < 32; off <<= 1) {
-      const float m2 = __shfl_xor_sync(0xffffffffu, acc.m, off);
-      const float S2 = __shfl_xor_sync(0xffffffffu, acc.S, off);
-      float4 a2[VPT];
+    // Merge the slots of the warp (lanes with the same column chunk), then
+    // the warps of the team: first the common maximum, then one rescale per
+    // state and plain sums, so that no merge waits on the one before it.
+    float M = acc.m;
+    for (int off = C; off < 32; off <<= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    {
+      const float f = M == -CUDART_INF_F ? 0.f : expf(acc.m - M);
+      acc.S *= f;
 #pragma unroll
       for (int k = 0; k < VPT; ++k) {
-        a2[k].x = __shfl_xor_sync(0xffffffffu, acc.a[k].x, off);
-        a2[k].y = __shfl_xor_sync(0xffffffffu, acc.a[k].y, off);
-        a2[k].z = __shfl_xor_sync(0xffffffffu, acc.a[k].z, off);
-        a2[k].w = __shfl_xor_sync(0xffffffffu, acc.a[k].w, off);
+        acc.a[k].x *= f;
+        acc.a[k].y *= f;
+        acc.a[k].z *= f;
+        acc.a[k].w *= f;
       }
-      lse_merge(acc, m2, S2, a2);
+      acc.m = M;
     }
-    // merge the warps of the team through shared memory
+    for (int off = C; off < 32; off <<= 1) {
+      acc.S += __shfl_xor_sync(0xffffffffu, acc.S, off);
+#pragma unroll
+      for (int k = 0; k < VPT; ++k) {
+        acc.a[k].x += __shfl_xor_sync(0xffffffffu, acc.a[k].x, off);
+        acc.a[k].y += __shfl_xor_sync(0xffffffffu, acc.a[k].y, off);
+        acc.a[k].z += __shfl_xor_sync(0xffffffffu, acc.a[k].z, off);
+        acc.a[k].w += __shfl_xor_sync(0xffffffffu, acc.a[k].w, off);
+      }
+    }
     if (W > 1) {
       if (lane < C) {
 #pragma unroll
@@ -185,13 +181,36 @@ __global__ void __launch_bounds__(kReduceThreads, 4)
         }
       }
       team_sync(g, W * 32);
-      if (wig == 0 && lane < C)
-        for (int w2 = 1; w2 < W; ++w2) {
-          float4 a2[VPT];
+      if (wig == 0 && lane < C) {
+        float Mt = acc.m;
 #pragma unroll
-          for (int k = 0; k < VPT; ++k) a2[k] = part_a[warp + w2][cl + C * k];
-          lse_merge(acc, part_m[warp + w2], part_S[warp + w2], a2);
+        for (int w2 = 1; w2 < 8; ++w2)
+          if (w2 < W) Mt = fmaxf(Mt, part_m[warp + w2]);
+        const float f0 = Mt == -CUDART_INF_F ? 0.f : expf(acc.m - Mt);
+        acc.S *= f0;
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) {
+          acc.a[k].x *= f0;
+          acc.a[k].y *= f0;
+          acc.a[k].z *= f0;
+          acc.a[k].w *= f0;
         }
+#pragma unroll
+        for (int w2 = 1; w2 < 8; ++w2) {
+          if (w2 >= W) break;
+          const float f = Mt == -CUDART_INF_F ? 0.f : expf(part_m[warp + w2] - Mt);
+          acc.S = fmaf(part_S[warp + w2], f, acc.S);
+#pragma unroll
+          for (int k = 0; k < VPT; ++k) {
+            const float4 a2 = part_a[warp + w2][cl + C * k];
+            acc.a[k].x = fmaf(a2.x, f, acc.a[k].x);
+            acc.a[k].y = fmaf(a2.y, f, acc.a[k].y);
+            acc.a[k].z = fmaf(a2.z, f, acc.a[k].z);
+            acc.a[k].w = fmaf(a2.w, f, acc.a[k].w);
+          }
+        }
+        acc.m = Mt;
+      }
     }
     if (!done && wig == 0 && lane < C) {
       OutT *out = static_cast<OutT *>(p.out) + row * D + col0;
