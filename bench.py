@@ -10,8 +10,18 @@ inputs already resident in HBM.  Prints ONE JSON line (rank 0).
                   [--math auto|tensor|simt] [--stages S]
 
 Metric: KV-read GB/s = (sum_s L_s * Hkv * D * elt * 2) / device time per step,
-and decode tokens/s = num_seqs / device time per step.  The L2 is flushed
-(a write larger than L2) before every timed step, outside the timed events.
+and decode tokens/s = num_seqs / device time per step.
+
+Timed region (``value``): K consecutive steps, as a decode pass runs them,
+one per layer: the steps cycle through ``layers`` copies of the workload
+(each its own K/V cache, queries and output; the block tables and lengths
+are shared, as across the layers of a model), enough copies that the cycle
+reads at least 4x the L2 size, so every step finds its K/V cold in L2 without
+a flush between steps.  Workloads too small for that (the tiny fp32 case)
+are timed step by step with an L2 flush before each step instead.
+``isolated`` reports the single-step latency too: the L2 flushed (a write
+and a read of 2x L2, outside the events) before every step, CUDA events
+around each step.
 
 Under torchrun (N > 1) every rank runs its own batch of the same shape on its
 own GPU (weak scaling; sequences are independent, there is no collective on
@@ -27,7 +37,9 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import math
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -46,7 +58,10 @@ UNIT = "GB/s"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 CHUNK_TOKENS = 4
-SECONDARY = "c3_long_100k"
+MAX_LAYERS = 64
+# the other workloads reported beside the headline, each timed like it
+SECONDARY = [("c3_long_100k", None), ("c2_gqa_batch8", None), ("c5_mixed_d256", 512),
+             ("c5_mixed_d256", 256), ("c1_tiny_fp32", None), ("gqa16_c4", None)]
 
 
 def parse_args(argv=None):
@@ -55,7 +70,8 @@ def parse_args(argv=None):
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="c4_batch256", choices=sorted(workloads.CONFIGS))
+    ap.add_argument("--workload", default="c4_batch256",
+                    choices=sorted(workloads.CONFIGS) + ["gqa16_c4"])
     ap.add_argument("--variant", choices=["auto", "v1", "v2"], default="auto")
     ap.add_argument("--math", choices=["auto", "tensor", "simt"], default="auto")
     ap.add_argument("--stages", type=int, default=0)
@@ -65,7 +81,7 @@ def parse_args(argv=None):
                          "Phase 1 (0: never, the library default)")
     ap.add_argument("--partition-size", type=int, default=0)
     ap.add_argument("--no-secondary", action="store_true",
-                    help="skip the extra long-context measurement")
+                    help="skip the other workloads, the query chunks and the CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args(argv)
 
@@ -195,6 +211,26 @@ def recorded_traffic(workload: str, kernel: str):
     return rec.get("dram_bytes_per_launch")
 
 
+def bench_case(name: str, partition_size=None, seed_offset: int = 0):
+    """A named workload: the five configurations, plus ``gqa16_c4`` (the
+    256-sequence lengths and cache shape with 32 query / 2 KV heads, groups
+    of 16 query heads per KV head)."""
+    if name == "gqa16_c4":
+        c = dict(workloads.CONFIGS["c4_batch256"])
+        c.pop("index")
+        c["num_kv_heads"] = 2
+        if partition_size:
+            c["partition_size"] = partition_size
+        return workloads.make_case("gqa16_c4", workloads.SEED_BASE + 77 + 1000 * seed_offset, **c)
+    return workloads.config_case(name, partition_size, seed_offset=seed_offset)
+
+
+def describe(name: str) -> str:
+    if name == "gqa16_c4":
+        return "256 seqs, L~U[512,3584], 32 q / 2 kv heads (G=16), D128, bf16, bs16"
+    return workloads.DESCRIPTIONS[name]
+
+
 def algorithmic_bytes(case, phase2_separate: bool) -> dict:
     """Bytes the dominant kernel must move: K and V of every token, the
     queries, the block-table entries it dereferences and seq_lens, and the
@@ -210,20 +246,60 @@ def algorithmic_bytes(case, phase2_separate: bool) -> dict:
     return {"kv": kv, "kernel": kv + q + table + out}
 
 
-class Runner:
-    """A workload resident on the GPU plus the call that runs one step."""
+def layers_for(kv_bytes: int, l2_bytes: int) -> int:
+    """Layer copies to cycle through so that one cycle reads >= 4x L2 of K/V;
+    0 when that would take more than MAX_LAYERS copies (timed with a flush)."""
+    n = max(2, math.ceil(4 * l2_bytes / max(kv_bytes, 1)))
+    return n if n <= MAX_LAYERS else 0
 
-    def __init__(self, case, device, variant, math, stages, ctas_per_sm=0, fuse_partitions=0):
+
+def workload_config(name: str, case, world: int, l2_note: str) -> dict:
+    """The `config` object: what the workload is, identical in both arms."""
+    return {
+        "workload": name, "description": describe(name),
+        "num_seqs": case.num_seqs, "num_heads": case.num_heads,
+        "num_kv_heads": case.num_kv_heads, "head_size": case.head_size,
+        "block_size": case.block_size, "partition_size": case.partition_size,
+        "dtype": dtype_name(case.dtype),
+        "mean_seq_len": round(float(case.seq_lens.double().mean()), 1),
+        "kv_bytes_per_step": case.kv_bytes(),
+        "l2": l2_note,
+        "parallelism": f"dp{world} (independent batches per GPU)",
+    }
+
+
+def l2_note_for(kv_bytes: int, l2_bytes: int) -> str:
+    n = layers_for(kv_bytes, l2_bytes)
+    if n:
+        return (f"inputs larger than L2: consecutive steps cycle through {n} layers' K/V caches "
+                f"({n * kv_bytes / 1e9:.2f} GB a cycle, L2 {l2_bytes / 1e6:.0f} MB); no flush "
+                "between steps")
+    return "flushed before every timed step (write then read of 2x L2 each, outside the events)"
+
+
+def dtype_name(dt) -> str:
+    return {torch.bfloat16: "bf16", torch.float16: "f16", torch.float32: "f32"}[dt]
+
+
+class Runner:
+    """A workload resident on the GPU, in `layers` copies (each its own K/V
+    cache, queries and output), plus the call that runs one step."""
+
+    def __init__(self, case, device, variant="auto", math="auto", stages=0, ctas_per_sm=0,
+                 fuse_partitions=0, layers=1):
         import paged_decode_attention_v2_gb300 as pa
         self.pa = pa
         self.case = case
         self.device = device
-        self.q = case.query.to(device)
-        self.kc = case.key_cache.to(device)
-        self.vc = case.value_cache.to(device)
+        q = case.query.to(device)
+        kc = case.key_cache.to(device)
+        vc = case.value_cache.to(device)
         self.bt = case.block_tables.to(device)
         self.sl = case.seq_lens.to(device)
-        self.out = torch.empty_like(self.q)
+        self.layer = [(q, kc, vc, torch.empty_like(q))]
+        for _ in range(1, max(1, layers)):
+            self.layer.append((q.clone(), kc.clone(), vc.clone(), torch.empty_like(q)))
+        self.q, self.kc, self.vc, self.out = self.layer[0]
         self.max_seq_len = case.max_seq_len
         self.variant = {"auto": pa.PA_VARIANT_AUTO, "v1": pa.PA_VARIANT_V1,
                         "v2": pa.PA_VARIANT_V2}[variant]
@@ -247,11 +323,13 @@ class Runner:
         self.has_phase2 = self.is_v2 and -(-self.max_seq_len // case.partition_size) > fuse
         self.kernels_per_step = 2 if self.has_phase2 else 1
 
-    def step(self, q=None, bt=None, sl=None, out=None, phase1_event=None):
-        self.pa.pa_forward(out if out is not None else self.out,
-                           q if q is not None else self.q, self.kc, self.vc,
-                           bt if bt is not None else self.bt,
-                           sl if sl is not None else self.sl,
+    @property
+    def layers(self) -> int:
+        return len(self.layer)
+
+    def step(self, layer=0, phase1_event=None):
+        q, kc, vc, out = self.layer[layer % len(self.layer)]
+        self.pa.pa_forward(out, q, kc, vc, self.bt, self.sl,
                            self.case.scale, self.case.partition_size, self.ws,
                            max_seq_len=self.max_seq_len, variant=self.variant, math=self.math,
                            num_stages=self.stages, phase1_event=phase1_event,
@@ -265,26 +343,39 @@ class Runner:
 
 class ChunkRunner:
     """The same cache as a Runner, queried with chunks of `tokens` tokens per
-    sequence (pa_chunks_forward)."""
+    sequence (pa_chunks_forward), in `layers` copies."""
 
-    def __init__(self, case, device, tokens):
+    def __init__(self, case, device, tokens, layers=1):
         import paged_decode_attention_v2_gb300 as pa
         self.pa = pa
         self.case = case
         q, qs = workloads.chunk_queries(case, tokens)
-        self.q = q.to(device)
+        q = q.to(device)
         self.q_start = qs.to(device)
-        self.kc = case.key_cache.to(device)
-        self.vc = case.value_cache.to(device)
+        kc = case.key_cache.to(device)
+        vc = case.value_cache.to(device)
         self.bt = case.block_tables.to(device)
         self.sl = case.seq_lens.to(device)
-        self.out = torch.empty_like(self.q)
+        self.layer = [(q, kc, vc, torch.empty_like(q))]
+        for _ in range(1, max(1, layers)):
+            self.layer.append((q.clone(), kc.clone(), vc.clone(), torch.empty_like(q)))
+        self.q = q
         self.tokens = tokens
-        self.ws = pa.alloc_workspace(self.q.shape[0], case.num_heads, case.head_size,
+        sm = torch.cuda.get_device_properties(device).multi_processor_count
+        self.is_v2 = bool(pa.pa_choose_v2(case.num_seqs, case.num_kv_heads, case.max_seq_len,
+                                          case.partition_size, sm))
+        self.has_phase2 = self.is_v2
+        self.kernels_per_step = 2 if self.is_v2 else 1
+        self.ws = pa.alloc_workspace(q.shape[0], case.num_heads, case.head_size,
                                      case.max_seq_len, case.partition_size, device=device)
 
-    def step(self, phase1_event=None, **_):
-        self.pa.pa_chunks_forward(self.out, self.q, self.kc, self.vc, self.bt, self.sl,
+    @property
+    def layers(self) -> int:
+        return len(self.layer)
+
+    def step(self, layer=0, phase1_event=None):
+        q, kc, vc, out = self.layer[layer % len(self.layer)]
+        self.pa.pa_chunks_forward(out, q, kc, vc, self.bt, self.sl,
                                   self.q_start, self.case.scale, self.case.partition_size,
                                   self.ws, max_seq_len=self.case.max_seq_len,
                                   max_chunk=self.tokens)
@@ -296,10 +387,9 @@ class ChunkRunner:
 
 
 class L2Flush:
-    """Evicts the workload from L2 before a timed step: writes a buffer of
-    twice the L2 size, then reads a second one, so that the dirty lines of the
-    write are written back here (outside the timed events) and not during
-    the timed kernel."""
+    """Evicts the workload from L2: writes a buffer of twice the L2 size, then
+    reads a second one, so that the dirty lines of the write are written back
+    here and not during the timed kernel."""
 
     def __init__(self, device):
         l2 = torch.cuda.get_device_properties(device).L2_cache_size
@@ -317,12 +407,29 @@ def l2_flush_buffer(device):
     return L2Flush(device)
 
 
+def _event():
+    return torch.cuda.Event(enable_timing=True)
+
+
+def time_consecutive(runner, steps, flush):
+    """K consecutive steps (cycling through the runner's layers) between one
+    pair of CUDA events on the launching stream; the L2 is flushed once
+    before the first.  Returns total ms."""
+    flush.zero_()
+    start, end = _event(), _event()
+    start.record()
+    for i in range(steps):
+        runner.step(layer=i)
+    end.record()
+    torch.cuda.synchronize()
+    return start.elapsed_time(end)
+
+
 def time_steps(runner, steps, flush, with_phase=False):
     """Per-step device times (ms) with CUDA events on the launching stream;
     the L2 flush runs before each step's start event."""
-    E = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
-    starts, ends = [E() for _ in range(steps)], [E() for _ in range(steps)]
-    mids = [E() for _ in range(steps)] if with_phase else None
+    starts, ends = [_event() for _ in range(steps)], [_event() for _ in range(steps)]
+    mids = [_event() for _ in range(steps)] if with_phase else None
     if mids:
         # torch creates the CUDA event at its first record(); do that here so
         # the handle handed to the library is live
@@ -341,10 +448,11 @@ def time_steps(runner, steps, flush, with_phase=False):
 
 
 def time_e2e(runner, steps, flush):
-    """The same step through the library's host-buffer C-ABI call
+    """The same steps through the library's host-buffer C-ABI call
     (pa_forward_host) from pinned HOST buffers: the query, block table and
-    lengths are copied in and the output copied out inside the timed region,
-    by the call itself."""
+    lengths are copied in and the output copied out by the call itself,
+    every step, inside the timed region.  Steps cycle through the runner's
+    layers like the device-resident steps."""
     c = runner.case
     pa = runner.pa
     hq = c.query.pin_memory()
@@ -352,42 +460,158 @@ def time_e2e(runner, steps, flush):
     hsl = c.seq_lens.pin_memory()
     hout = torch.empty(c.query.shape, dtype=c.query.dtype).pin_memory()
     staging = pa.alloc_staging(hq, hbt, device=runner.device)
-    E = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
-    starts, ends = [E() for _ in range(steps)], [E() for _ in range(steps)]
-    for i in range(steps):
-        flush.zero_()
-        starts[i].record()
-        pa.pa_forward_host(hout, hq, runner.kc, runner.vc, hbt, hsl, c.scale,
-                           c.partition_size, staging, runner.ws,
-                           max_seq_len=runner.max_seq_len, variant=runner.variant,
+
+    def call(i):
+        _, kc, vc, _ = runner.layer[i % runner.layers]
+        pa.pa_forward_host(hout, hq, kc, vc, hbt, hsl, c.scale, c.partition_size, staging,
+                           runner.ws, max_seq_len=runner.max_seq_len, variant=runner.variant,
                            math=runner.math, num_stages=runner.stages,
                            ctas_per_sm=runner.ctas_per_sm,
                            fuse_partitions=runner.fuse_partitions)
-        ends[i].record()
+    for i in range(3):
+        call(i)
     torch.cuda.synchronize()
-    ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     h2d = hq.numel() * hq.element_size() + hbt.numel() * 4 + hsl.numel() * 4
     d2h = hout.numel() * hout.element_size()
-    return ms, h2d, d2h
+    if runner.layers > 1:
+        flush.zero_()
+        start, end = _event(), _event()
+        start.record()
+        for i in range(steps):
+            call(i)
+        end.record()
+        torch.cuda.synchronize()
+        return start.elapsed_time(end) / steps, h2d, d2h
+    ms = []
+    for i in range(steps):
+        flush.zero_()
+        start, end = _event(), _event()
+        start.record()
+        call(i)
+        end.record()
+        torch.cuda.synchronize()
+        ms.append(start.elapsed_time(end))
+    return statistics.mean(ms), h2d, d2h
 
 
-def cpu_oracle_sample(case, target_s=3.0):
-    """Time the oracle, as it stands, on the first n sequences of the case,
-    n sized for a few seconds of wall time on all host cores."""
+def measure(name, case, runner, flush, peak, steps, iso_steps):
+    """One workload as a `secondary` entry: consecutive steps (or flushed
+    steps when it is too small to cycle through L2), the isolated flushed
+    step, and the Phase 1 kernel's share of it."""
+    for _ in range(5):
+        runner.step()
+    if runner.layers > 1:
+        ms = time_consecutive(runner, steps, flush) / steps
+    else:
+        ms = None
+    iso, _ = time_steps(runner, iso_steps, flush)
+    p1 = None
+    if runner.has_phase2:
+        _, p1 = time_steps(runner, max(iso_steps // 2, 20), flush, with_phase=True)
+    runner.check_status()
+    iso_ms = statistics.median(iso)
+    step_ms = ms if ms is not None else iso_ms
+    kv = case.kv_bytes()
+    gbs = kv / (step_ms / 1e3) / 1e9
+    alg = algorithmic_bytes(case, runner.has_phase2)
+    entry = {
+        "value": round(gbs, 2), "unit": UNIT, "frac_of_peak": round(gbs / peak, 4),
+        "ms_per_step": round(step_ms, 5),
+        "tokens_per_s": round(case.num_seqs / (step_ms / 1e3), 1),
+        "timing": (f"{steps} consecutive steps over {runner.layers} layers' caches"
+                   if ms is not None else "flushed steps (too small to cycle through L2)"),
+        "isolated": {"ms_per_step": round(iso_ms, 5),
+                     "value": round(kv / (iso_ms / 1e3) / 1e9, 2),
+                     "frac_of_peak": round(kv / (iso_ms / 1e3) / 1e9 / peak, 4)},
+        "variant": "v2" if runner.is_v2 else "v1",
+        "kv_bytes_per_step": kv,
+        "description": describe(name),
+    }
+    if p1:
+        p1m = statistics.median(p1)
+        entry["phase1_ms"] = round(p1m, 5)
+        entry["phase1_frac_of_peak"] = round(alg["kernel"] / (p1m / 1e3) / 1e9 / peak, 4)
+    return entry
+
+
+# ---------------------------------------------------------------------------
+# CPU baseline (the oracle, as it stands)
+
+def cpu_model() -> str:
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return platform.machine()
+
+
+def cpu_oracle_sample(case, target_s=3.0, nthreads=0):
+    """The first n sequences of the case, n sized for about target_s of
+    oracle wall time on nthreads host threads (0: all)."""
     import oracle
-    nt = oracle.max_threads()
     n = 1
     while True:
         sub = workloads.sub_batch(case, n)
         t0 = time.perf_counter()
         oracle.attention(sub.query, sub.key_cache, sub.value_cache, sub.block_tables,
-                         sub.seq_lens, sub.scale)
+                         sub.seq_lens, sub.scale, nthreads=nthreads)
         dt = time.perf_counter() - t0
         if dt >= target_s or n >= case.num_seqs:
             break
         n = min(case.num_seqs, max(n + 1, int(n * min(8.0, 1.2 * target_s / max(dt, 1e-3)))))
-    return sub, dt, nt
+    return sub
 
+
+def time_oracle(sub, runs=3, nthreads=0):
+    """Median wall time (steady clock) of `runs` oracle calls on sub."""
+    import oracle
+    ts = []
+    for _ in range(runs):
+        t0 = time.perf_counter()
+        oracle.attention(sub.query, sub.key_cache, sub.value_cache, sub.block_tables,
+                         sub.seq_lens, sub.scale, nthreads=nthreads)
+        ts.append(time.perf_counter() - t0)
+    return statistics.median(ts)
+
+
+def cpu_baseline(name, case, target_s=3.0):
+    """The oracle on all host cores, median of 3, on a bounded sample of the
+    headline workload, plus one thread on the three small configurations."""
+    import oracle
+    oracle.build()
+    nt = oracle.max_threads()
+    sub = cpu_oracle_sample(case, target_s)
+    dt = time_oracle(sub, 3)
+    single = {}
+    for cname in ("c1_tiny_fp32", "c2_gqa_batch8", "c3_long_100k"):
+        c = case if cname == name else workloads.config_case(cname)
+        s1 = cpu_oracle_sample(c, 1.0, nthreads=1)
+        d1 = time_oracle(s1, 3, nthreads=1)
+        single[cname] = {"value": round(s1.kv_bytes() / d1 / 1e9, 4), "unit": UNIT,
+                         "tokens_per_s": round(s1.num_seqs / d1, 2),
+                         "sample": f"first {s1.num_seqs} of {c.num_seqs} sequences, "
+                                   f"median of 3 runs of {d1:.3f} s"}
+    return {
+        "value": round(sub.kv_bytes() / dt / 1e9, 4), "unit": UNIT, "cores": nt, "kind": "oracle",
+        "sample": f"first {sub.num_seqs} of {case.num_seqs} sequences of {name} "
+                  f"({sub.kv_bytes()} KV bytes), fp64 C oracle, median of 3 runs of {dt:.3f} s",
+        "tokens_per_s": round(sub.num_seqs / dt, 2),
+        "cpu_model": cpu_model(), "nproc": os.cpu_count(),
+        "single_thread": single,
+    }
+
+
+# ---------------------------------------------------------------------------
 
 def run_ours(args):
     rank, world, local = dist_env()
@@ -401,45 +625,61 @@ def run_ours(args):
         build_lib.build()
     barrier(world)
 
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
     P = args.partition_size or None
-    case = workloads.config_case(args.workload, P, seed_offset=rank)
+    case = bench_case(args.workload, P, seed_offset=rank)
     runner = Runner(case, device, args.variant, args.math, args.stages, args.ctas_per_sm,
-                    args.fuse_partitions)
+                    args.fuse_partitions, layers=max(1, layers_for(case.kv_bytes(), l2)))
     flush = l2_flush_buffer(device)
-    for _ in range(args.warmup):
-        runner.step()
+    for i in range(args.warmup):
+        runner.step(layer=i)
     runner.check_status()
 
     sampler = ClockSampler(local)
     barrier(world)
     torch.cuda.synchronize()
     sampler.start()
-    step_ms, _ = time_steps(runner, args.steps, flush)
-    torch.cuda.synchronize()
-    barrier(world)
-    # per-kernel breakdown and end-to-end timing, still under load
-    brk_steps = min(args.steps, 500)
-    brk_ms, phase1_ms = time_steps(runner, brk_steps, flush, with_phase=runner.has_phase2)
-    e2e_ms, h2d, d2h = time_e2e(runner, min(args.steps, 500), flush)
+    # ---- the timed region: K consecutive steps (or K flushed steps)
+    if runner.layers > 1:
+        flush.zero_()
+        torch.cuda.synchronize()
+        barrier(world)
+        start, end = _event(), _event()
+        start.record()
+        for i in range(args.steps):
+            runner.step(layer=i)
+        end.record()
+        torch.cuda.synchronize()
+        barrier(world)
+        total_ms = start.elapsed_time(end)
+        step_ms = [total_ms / args.steps] * args.steps
+    else:
+        step_ms, _ = time_steps(runner, args.steps, flush)
+        total_ms = sum(step_ms)
+        torch.cuda.synchronize()
+        barrier(world)
+    # per-kernel breakdown, isolated steps and end-to-end timing, still under load
+    brk_steps = min(max(args.steps, 50), 500)
+    iso_ms, phase1_ms = time_steps(runner, brk_steps, flush, with_phase=runner.has_phase2)
+    e2e_ms, h2d, d2h = time_e2e(runner, min(max(args.steps, 50), 500), flush)
     clocks = sampler.stop()
     runner.check_status()
 
-    total_s = sum(step_ms) / 1e3
-    total_s_max = reduce_over_ranks(total_s, "max", world, device)
+    total_s_max = reduce_over_ranks(total_ms / 1e3, "max", world, device)
     kv_all = reduce_over_ranks(float(case.kv_bytes()), "sum", world, device)
     seqs_all = reduce_over_ranks(float(case.num_seqs), "sum", world, device)
-    e2e_s_max = reduce_over_ranks(sum(e2e_ms) / 1e3, "max", world, device)
+    e2e_s_max = reduce_over_ranks(e2e_ms / 1e3, "max", world, device)
     value = kv_all * args.steps / total_s_max / 1e9
     if rank != 0:
         return None
 
     peak, peak_kind = measured_hbm_peak()
     alg = algorithmic_bytes(case, runner.has_phase2)
-    dom_ms = statistics.mean(phase1_ms) if phase1_ms else statistics.mean(brk_ms)
+    dom_ms = statistics.mean(phase1_ms) if phase1_ms else statistics.mean(iso_ms)
     achieved = alg["kernel"] / (dom_ms / 1e3) / 1e9
     kernel_name = ("pa_attn_kernel(phase1)" if runner.has_phase2 else
                    "pa_attn_kernel(v2, combine fused)" if runner.is_v2 else "pa_attn_kernel(v1)")
-    mean_ms = statistics.mean(step_ms)
+    iso_med = statistics.median(iso_ms)
     line = {
         "metric": METRIC,
         "value": round(value, 2),
@@ -451,25 +691,21 @@ def run_ours(args):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": {torch.bfloat16: "bf16", torch.float16: "f16",
-                  torch.float32: "f32"}[case.dtype],
+        "dtype": dtype_name(case.dtype),
         "data": "synthetic (seeded N(0,1) Q/K/V, shuffled paged pool)",
-        "config": {
-            "workload": args.workload,
-            "description": workloads.DESCRIPTIONS[args.workload],
-            "num_seqs": case.num_seqs, "num_heads": case.num_heads,
-            "num_kv_heads": case.num_kv_heads, "head_size": case.head_size,
-            "block_size": case.block_size, "partition_size": case.partition_size,
-            "mean_seq_len": round(float(case.seq_lens.double().mean()), 1),
-            "kv_bytes_per_step": case.kv_bytes(),
-            "variant": "v2" if runner.is_v2 else "v1", "math": args.math,
-            "l2": "flushed before every timed step (write then read of 2x L2 each, outside the events)",
-            "parallelism": f"dp{world} (independent batches per GPU)",
-        },
+        "config": workload_config(args.workload, case, world, l2_note_for(case.kv_bytes(), l2)),
+        "implementation": {"variant": "v2" if runner.is_v2 else "v1", "math": args.math,
+                           "layers": runner.layers},
         "tokens_per_s": round(seqs_all * args.steps / total_s_max, 1),
+        "frac_of_peak": round(value / peak / world, 4),
         "frac_of_nominal_8tbs": round(value / NOMINAL_HBM_GBS / world, 4),
-        "step_ms_p10_p50_p90": [round(x, 5) for x in statistics.quantiles(step_ms, n=10)[::4]]
-        if len(step_ms) >= 10 else None,
+        "isolated": {"ms_per_step": round(iso_med, 5),
+                     "value": round(case.kv_bytes() / (iso_med / 1e3) / 1e9, 2),
+                     "frac_of_peak": round(case.kv_bytes() / (iso_med / 1e3) / 1e9 / peak, 4),
+                     "step_ms_p10_p50_p90": [round(x, 5) for x in
+                                             statistics.quantiles(iso_ms, n=10)[::4]],
+                     "how": "L2 flushed before every step, CUDA events around each step "
+                            "(includes the launch latency of an isolated call)"},
         "roofline": {
             "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
             "unit": "GB/s", "frac": round(achieved / peak, 4),
@@ -477,59 +713,46 @@ def run_ours(args):
             "kernel": kernel_name, "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
             if peak_kind == "measured" else "fallback 6.8 TB/s",
             "alg_bytes_per_launch": alg["kernel"], "kernel_ms": round(dom_ms, 5),
+            "kernel_ms_how": "isolated flushed steps: CUDA event before the step to the event "
+                             "the library records between Phase 1 and Phase 2",
         },
-        "e2e": {"value": round(kv_all * len(e2e_ms) / e2e_s_max / 1e9, 2), "unit": UNIT,
+        "e2e": {"value": round(kv_all / e2e_s_max / 1e9, 2), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": round(statistics.mean(e2e_ms), 5)},
+                "ms_per_step": round(e2e_ms, 5)},
         "gpu_launches": runner.kernels_per_step * args.steps,
         "clocks": clocks,
     }
     if phase1_ms:
         line["phase_ms"] = {"phase1": round(statistics.mean(phase1_ms), 5),
-                            "phase2_incl_gap": round(statistics.mean(brk_ms)
+                            "phase2_incl_gap": round(statistics.mean(iso_ms)
                                                      - statistics.mean(phase1_ms), 5)}
-    if world == 1 and not args.no_secondary and args.workload != SECONDARY:
-        sec = workloads.config_case(SECONDARY)
-        r2 = Runner(sec, device, "auto", "auto", 0)
-        for _ in range(max(args.warmup, 3)):
-            r2.step()
-        # the step as a whole (Phase 2 chained to Phase 1), then a second pass
-        # with an event between the phases for the split
-        ms2, _ = time_steps(r2, min(args.steps, 500), flush)
-        p1 = None
-        if r2.has_phase2:
-            _, p1 = time_steps(r2, min(args.steps, 200), flush, with_phase=True)
-        r2.check_status()
-        gbs = sec.kv_bytes() / (statistics.mean(ms2) / 1e3) / 1e9
-        line["secondary"] = {SECONDARY: {
-            "value": round(gbs, 2), "unit": UNIT, "frac_of_peak": round(gbs / peak, 4),
-            "ms_per_step": round(statistics.mean(ms2), 5),
-            "variant": "v2" if r2.is_v2 else "v1",
-            "phase1_ms": round(statistics.mean(p1), 5) if p1 else None}}
-        del r2
+    del runner
+    torch.cuda.empty_cache()
     if world == 1 and not args.no_secondary:
+        sec = {}
+        for name, Ps in SECONDARY:
+            if name == args.workload and (Ps or None) == P:
+                continue
+            c2 = bench_case(name, Ps)
+            r2 = Runner(c2, device, layers=max(1, layers_for(c2.kv_bytes(), l2)))
+            key = name if Ps is None else f"{name}_P{Ps}"
+            sec[key] = measure(name, c2, r2, flush, peak, 200, 200)
+            del r2
+            torch.cuda.empty_cache()
+        line["secondary"] = sec
         # query chunks (speculative-decoding verification shape): the headline
         # cache with 4-token chunks per sequence
-        cr = ChunkRunner(case, device, CHUNK_TOKENS)
-        for _ in range(max(args.warmup, 3)):
-            cr.step()
-        msc, _ = time_steps(cr, min(args.steps, 500), flush)
-        cr.check_status()
-        mc = statistics.mean(msc)
-        line["chunks"] = {
-            "workload": f"{args.workload}, {CHUNK_TOKENS}-token query chunks",
-            "value": round(case.kv_bytes() / (mc / 1e3) / 1e9, 2), "unit": UNIT,
-            "frac_of_peak": round(case.kv_bytes() / (mc / 1e3) / 1e9 / peak, 4),
-            "ms_per_step": round(mc, 5),
-            "query_rows_per_s": round(cr.q.shape[0] / (mc / 1e3), 1)}
+        cr = ChunkRunner(case, device, CHUNK_TOKENS,
+                         layers=max(1, layers_for(case.kv_bytes(), l2)))
+        ce = measure(args.workload, case, cr, flush, peak, 200, 200)
+        ce["workload"] = f"{args.workload}, {CHUNK_TOKENS}-token query chunks"
+        ce["query_rows_per_s"] = round(cr.q.shape[0] / (ce["ms_per_step"] / 1e3), 1)
+        ce.pop("tokens_per_s", None)
+        line["chunks"] = ce
         del cr
-    if world == 1 and not args.no_cpu_baseline:
-        sub, dt, nt = cpu_oracle_sample(case)
-        line["cpu_baseline"] = {
-            "value": round(sub.kv_bytes() / dt / 1e9, 4), "unit": UNIT, "cores": nt,
-            "kind": "oracle",
-            "sample": f"first {sub.num_seqs} of {case.num_seqs} sequences of {args.workload} "
-                      f"({sub.kv_bytes()} KV bytes), fp64 C oracle, one run, {dt:.2f} s wall"}
+        torch.cuda.empty_cache()
+    if world == 1 and not args.no_cpu_baseline and not args.no_secondary:
+        line["cpu_baseline"] = cpu_baseline(args.workload, case)
     return line
 
 
@@ -540,12 +763,21 @@ def run_reference(args):
     import oracle
     oracle.build()
     P = args.partition_size or None
-    case = workloads.config_case(args.workload, P)
+    case = bench_case(args.workload, P)
+    l2 = 0
+    try:
+        if torch.cuda.is_available():
+            l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    except Exception:
+        l2 = 0
+    l2 = l2 or 126 * 1024 * 1024
+    nt = oracle.max_threads()
     # size the per-step sample so that warmup + steps end within ~2 minutes
-    sub, dt, nt = cpu_oracle_sample(case, target_s=0.05)
+    probe = cpu_oracle_sample(case, target_s=0.05)
+    dt = time_oracle(probe, 1)
     budget = 120.0
     per_step = budget / max(1, args.steps + args.warmup)
-    n = max(1, min(case.num_seqs, int(sub.num_seqs * per_step / max(dt, 1e-6))))
+    n = max(1, min(case.num_seqs, int(probe.num_seqs * per_step / max(dt, 1e-6))))
     sample = workloads.sub_batch(case, n)
     run = lambda: oracle.attention(sample.query, sample.key_cache, sample.value_cache,  # noqa
                                    sample.block_tables, sample.seq_lens, sample.scale)
@@ -564,11 +796,10 @@ def run_reference(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(mean_s * 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f64", "data": "synthetic (seeded N(0,1) Q/K/V, shuffled paged pool)",
-        "config": {"workload": args.workload,
-                   "description": workloads.DESCRIPTIONS[args.workload],
-                   "sample_seqs": n, "num_seqs": case.num_seqs},
+        "config": workload_config(args.workload, case, world, l2_note_for(case.kv_bytes(), l2)),
         "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": nt, "kind": "oracle",
-                         "sample": f"first {n} of {case.num_seqs} sequences per step"},
+                         "sample": f"first {n} of {case.num_seqs} sequences per step",
+                         "cpu_model": cpu_model()},
         "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }

@@ -164,6 +164,52 @@ pa_status_t pa_forward(void *out, const void *query, const void *key_cache,
                        void *workspace, size_t workspace_bytes, void *stream,
                        const pa_options_t *opts);
 
+/* The two phases of V2 as separate calls, for splitting long sequences over
+ * several GPUs (context parallelism).  The "paged_attention_v2" commit note
+ * (project_6, commit 96f4baf "Dockerfile", section "Implementation") defines
+ * Phase 1 per partition and Phase 2 as the log-sum-exp reduction over a
+ * sequence's partitions; the partitions are independent until Phase 2, so
+ * GPU r can run Phase 1 over its own range of partitions, the GPUs exchange
+ * their partials (one all-gather of max_logits, exp_sums and tmp_out slots,
+ * done by the caller), and Phase 2 over the gathered slots gives the
+ * single-GPU result.
+ *
+ * pa_v2_partials: Phase 1 only, for the partitions p with
+ *   part_begin <= p < min(part_end, ceil(seq_lens[s] / partition_size))
+ * of every sequence s.  It writes their max_logits / exp_sums / tmp_out
+ * slots of the workspace (the layout of pa_workspace_layout, sized by
+ * pa_workspace_bytes for the whole sequences) and nothing else: slots of
+ * other partitions keep their contents, and there is no output.  Block-table
+ * entries of pages outside the range are never read, so a GPU that holds only
+ * its own range's pages may pass -1 there.  The arguments are those of
+ * pa_v2_forward (seq_lens are the whole lengths), without out, plus
+ * 0 <= part_begin <= part_end (PA_ERR_INVALID_ARG otherwise; part_end may
+ * exceed the partition count).  [0, INT32_MAX) is Phase 1 of pa_v2_forward.
+ * Errors as pa_v2_forward; device-detected ones land in this workspace's
+ * status word. */
+pa_status_t pa_v2_partials(const void *query, const void *key_cache,
+                           const void *value_cache, const int32_t *block_tables,
+                           const int32_t *seq_lens, int num_seqs, int num_heads,
+                           int num_kv_heads, int head_size, int num_blocks,
+                           int block_size, int max_blocks_per_seq,
+                           int max_seq_len, float scale, int partition_size,
+                           int dtype, int part_begin, int part_end,
+                           void *workspace, size_t workspace_bytes,
+                           void *stream);
+
+/* pa_v2_combine: Phase 2 only.  For every sequence s and head h, the
+ * log-sum-exp combine of the slots of partitions 0 .. ceil(seq_lens[s] /
+ * partition_size) - 1 in the workspace, written to out[s][h] in dtype (zeros
+ * for an empty sequence).  Every one of those slots must hold a Phase 1
+ * result (pa_v2_partials here, or slots copied in from other GPUs); the
+ * workspace is only read.  seq_lens and out on the device, layouts and the
+ * other arguments as pa_v2_forward; head_size, dtype and partition_size are
+ * checked as there.  Enqueued on `stream` after whatever precedes it. */
+pa_status_t pa_v2_combine(void *out, const int32_t *seq_lens, int num_seqs,
+                          int num_heads, int head_size, int max_seq_len,
+                          int partition_size, int dtype, const void *workspace,
+                          size_t workspace_bytes, void *stream);
+
 /* Multi-token queries over the paged cache: the query of sequence s is a
  * chunk of its LAST n_s = q_start[s+1] - q_start[s] cached tokens (for
  * example draft tokens to verify, or a small prefill chunk whose keys and

@@ -43,7 +43,7 @@ EXPORTS = ("pa_workspace_bytes", "pa_workspace_layout", "pa_workspace_init",
            "pa_v1_forward", "pa_v2_forward", "pa_forward", "pa_choose_v2",
            "pa_read_device_status", "pa_status_string", "pa_last_cuda_error",
            "pa_version", "pa_v2_forward_noalloc", "pa_host_staging_bytes", "pa_forward_host",
-           "pa_chunks_forward")
+           "pa_chunks_forward", "pa_v2_partials", "pa_v2_combine")
 
 
 class PAError(RuntimeError):
@@ -89,6 +89,10 @@ def load_library(path: str = LIB_PATH):
             f = getattr(lib, name)
             f.restype = ci
             f.argtypes = _FWD_ARGS
+        lib.pa_v2_partials.restype = ci
+        lib.pa_v2_partials.argtypes = (_FWD_ARGS[1:17] + [ci, ci] + _FWD_ARGS[17:])
+        lib.pa_v2_combine.restype = ci
+        lib.pa_v2_combine.argtypes = [vp, vp] + [ci] * 6 + [vp, cs, vp]
         lib.pa_v2_forward_noalloc.restype = ci
         lib.pa_v2_forward_noalloc.argtypes = _FWD_ARGS[:17] + [vp]
         lib.pa_forward.restype = ci
@@ -207,6 +211,31 @@ def pa_v2_forward(out, query, key_cache, value_cache, block_tables, seq_lens, sc
     _check(load_library().pa_v2_forward(*_fwd_args(
         out, query, key_cache, value_cache, block_tables, seq_lens, scale, partition_size,
         workspace, max_seq_len, stream)), "pa_v2_forward")
+
+
+def pa_v2_partials(query, key_cache, value_cache, block_tables, seq_lens, scale,
+                   partition_size, workspace, part_begin=0, part_end=2 ** 31 - 1,
+                   max_seq_len=None, stream=None) -> None:
+    """Phase 1 of V2 over partitions [part_begin, part_end) of every sequence,
+    into their workspace slots (see include/pa.h)."""
+    a = _fwd_args(query, query, key_cache, value_cache, block_tables, seq_lens, scale,
+                  partition_size, workspace, max_seq_len, stream)
+    _check(load_library().pa_v2_partials(*a[1:17], int(part_begin), int(part_end), *a[17:]),
+           "pa_v2_partials")
+
+
+def pa_v2_combine(out, seq_lens, partition_size, workspace, max_seq_len, num_kv_heads=None,
+                  stream=None) -> None:
+    """Phase 2 of V2 alone: out [B, H, D] from the partials in the workspace
+    (see include/pa.h).  ``num_kv_heads`` is unused (Phase 2 works per query
+    head) and accepted for symmetry with the forward calls."""
+    if out.dtype not in _DTYPES:
+        raise ValueError(f"unsupported dtype {out.dtype}")
+    B, H, D = out.shape
+    _check(load_library().pa_v2_combine(
+        _ptr(out), _ptr(seq_lens), B, H, D, int(max_seq_len), int(partition_size),
+        _DTYPES[out.dtype], _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _stream_handle(stream)), "pa_v2_combine")
 
 
 def pa_v2_forward_noalloc(out, query, key_cache, value_cache, block_tables, seq_lens, scale,

@@ -1,6 +1,7 @@
 // libpa C ABI: argument checks, the V1/V2 choice, the launch plan (pipeline
 // depth, grids, TMA descriptors) and the kernel launches.
 #include <cudaTypedefs.h>
+#include <limits.h>
 #include <math.h>
 #include <stdio.h>
 #include <string.h>
@@ -187,6 +188,10 @@ struct Call {
   const int32_t *q_start;
   int num_rows;
   int max_chunk;
+  // V2 split into its phases (pa_v2_partials / pa_v2_combine): the phases to
+  // run (bit 0: Phase 1, bit 1: Phase 2) and Phase 1's range of partitions
+  int phases = 3;
+  int part_begin = 0, part_end = INT_MAX;
 };
 
 // Rows of query (and output) and of the V2 workspace: sequences, or the query
@@ -234,6 +239,9 @@ pa_status_t check_args(const Call &c, bool need_v2) {
     return PA_ERR_UNSUPPORTED;
   if (need_v2 && max_parts_of(c.max_seq_len, c.partition_size) > kMaxReduceParts)
     return PA_ERR_UNSUPPORTED;
+  if (c.part_begin < 0 || c.part_end < c.part_begin) return PA_ERR_INVALID_ARG;
+  if ((c.part_begin != 0 || c.part_end != INT_MAX) && (!need_v2 || c.q_start))
+    return PA_ERR_INVALID_ARG;  // a range of partitions is a V2 decode notion
   if (!c.out || !c.query || !c.key_cache || !c.value_cache || !c.block_tables || !c.seq_lens ||
       !c.workspace)
     return PA_ERR_INVALID_ARG;
@@ -244,6 +252,25 @@ pa_status_t check_args(const Call &c, bool need_v2) {
   const size_t need = need_v2 ? pa_workspace_bytes(query_rows(c), c.num_heads, c.head_size,
                                                    c.max_seq_len, c.partition_size)
                               : (size_t)kStatusBytes;
+  if (need == 0) return PA_ERR_INVALID_ARG;
+  if (c.workspace_bytes < need) return PA_ERR_WORKSPACE_TOO_SMALL;
+  return PA_OK;
+}
+
+// Checks of a Phase-2-only call (pa_v2_combine): no query, caches or tables.
+pa_status_t check_combine_args(const Call &c) {
+  if (c.dtype != PA_DTYPE_F32 && c.dtype != PA_DTYPE_BF16 && c.dtype != PA_DTYPE_F16)
+    return PA_ERR_INVALID_ARG;
+  if (c.num_seqs < 0 || c.num_heads < 1 || c.max_seq_len < 0 || c.partition_size < 1)
+    return PA_ERR_INVALID_ARG;
+  if (c.head_size != 64 && c.head_size != 128 && c.head_size != 256) return PA_ERR_UNSUPPORTED;
+  if (c.partition_size % 64 || c.partition_size > 8192) return PA_ERR_UNSUPPORTED;
+  if (max_parts_of(c.max_seq_len, c.partition_size) > kMaxReduceParts) return PA_ERR_UNSUPPORTED;
+  if (!c.out || !c.seq_lens || !c.workspace) return PA_ERR_INVALID_ARG;
+  if (!aligned(c.out, 16) || !aligned(c.seq_lens, 4) || !aligned(c.workspace, 256))
+    return PA_ERR_INVALID_ARG;
+  const size_t need = pa_workspace_bytes(c.num_seqs, c.num_heads, c.head_size, c.max_seq_len,
+                                         c.partition_size);
   if (need == 0) return PA_ERR_INVALID_ARG;
   if (c.workspace_bytes < need) return PA_ERR_WORKSPACE_TOO_SMALL;
   return PA_OK;
@@ -342,6 +369,28 @@ pa_status_t plan_phase2(const Call &c, const AttnParams &p, const DeviceFacts *d
   return PA_OK;
 }
 
+// Launch a planned Phase 2 kernel, chained to the previous kernel of the
+// stream by programmatic dependent launch (its own wait holds it until that
+// kernel has completed).
+pa_status_t launch_phase2(const Phase2Plan &plan, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg;
+  memset(&cfg, 0, sizeof cfg);
+  cfg.gridDim = dim3((unsigned)plan.ctas, 1, 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  ReduceParams r = plan.r;
+  void *rargs[1] = {&r};
+  cudaError_t e = cudaLaunchKernelExC(&cfg, plan.fn, rargs);
+  if (e != cudaSuccess) return fail_cuda("launch reduce kernel", e);
+  return PA_OK;
+}
+
 pa_status_t launch(const Call &c, bool v2, const pa_options_t &opt) {
   DeviceFacts *dev = nullptr;
   pa_status_t st = device_facts(&dev);
@@ -436,11 +485,16 @@ pa_status_t launch(const Call &c, bool v2, const pa_options_t &opt) {
   p.range_tokens = v2 ? c.partition_size : (c.max_seq_len > 0 ? c.max_seq_len : 1);
   p.max_parts = max_parts > 0 ? max_parts : 1;
   p.write_partials = v2 ? 1 : 0;
+  p.part_begin = c.part_begin;
+  p.part_end = c.part_end;
+  const bool phase1 = (c.phases & 1) != 0;
+  const bool phase2 = (c.phases & 2) != 0;
   if (v2) {
     // Off unless asked for: on the workloads measured so far the separate
     // Phase 2 kernel costs less than the per-item handshake of the fused one.
     const int fuse = opt.fuse_partitions > 0 ? opt.fuse_partitions : 0;
     p.fuse_limit = fuse > kFuseLimitMax ? kFuseLimitMax : fuse;
+    if (!phase1 || !phase2) p.fuse_limit = 0;  // the phases run apart
     p.group_count = reinterpret_cast<int *>(ws + off[4]);
     // chunk mode: no fused combine; the counters region holds the rows' limits
     if (chunk) {
@@ -464,14 +518,16 @@ pa_status_t launch(const Call &c, bool v2, const pa_options_t &opt) {
   // Phase 1's CTAs can retire without a last-CTA-out handshake.
   const long long prows = (long long)query_rows(c) * c.num_heads;
   const bool run_p2 =
-      v2 && prows > 0 &&
+      v2 && phase2 && prows > 0 &&
       !(p.fuse_limit > 0 && max_parts_of(c.max_seq_len, c.partition_size) <= p.fuse_limit);
   Phase2Plan plan;
   if (run_p2) {
     st = plan_phase2(c, p, dev, prows, &plan);
     if (st != PA_OK) return st;
-    plan.r.sched = p.sched;
-    p.sched_reset_later = 1;
+    if (phase1) {
+      plan.r.sched = p.sched;
+      p.sched_reset_later = 1;
+    }
   }
 
   st = ensure_smem(k.fn, smem);
@@ -484,11 +540,15 @@ pa_status_t launch(const Call &c, bool v2, const pa_options_t &opt) {
   if (st != PA_OK) return st;
   if (per_sm < 1) return PA_ERR_UNSUPPORTED;
   if (opt.ctas_per_sm > 0 && opt.ctas_per_sm < per_sm) per_sm = opt.ctas_per_sm;
-  const long long max_items = (long long)c.num_seqs * c.num_kv_heads * p.max_parts *
-                              (chunk ? (c.max_chunk + p.chunk_tokens - 1) / p.chunk_tokens : 1);
+  const long long range_parts =
+      v2 ? (long long)(c.part_end < p.max_parts ? c.part_end : p.max_parts) - c.part_begin
+         : p.max_parts;
+  const long long max_items =
+      (long long)c.num_seqs * c.num_kv_heads * (range_parts > 0 ? range_parts : 0) *
+      (chunk ? (c.max_chunk + p.chunk_tokens - 1) / p.chunk_tokens : 1);
   long long grid = (long long)per_sm * dev->sm_count;
   if (grid > max_items) grid = max_items;
-  if (grid > 0) {
+  if (phase1 && grid > 0) {
     cudaLaunchConfig_t cfg;
     memset(&cfg, 0, sizeof cfg);
     cfg.gridDim = dim3((unsigned)grid, 1, 1);
@@ -509,31 +569,43 @@ pa_status_t launch(const Call &c, bool v2, const pa_options_t &opt) {
   }
   if (!run_p2) return PA_OK;
 
-  if (opt.phase1_event) {
+  if (opt.phase1_event && phase1) {
     cudaError_t e = cudaEventRecord(static_cast<cudaEvent_t>(opt.phase1_event), c.stream);
     if (e != cudaSuccess) {
       cudaMemsetAsync(p.sched, 0, 2 * sizeof(int), c.stream);  // Phase 2 will not reset it
       return fail_cuda("cudaEventRecord(phase1_event)", e);
     }
   }
-  cudaLaunchConfig_t cfg;
-  memset(&cfg, 0, sizeof cfg);
-  cfg.gridDim = dim3((unsigned)plan.ctas, 1, 1);
-  cfg.blockDim = dim3(256, 1, 1);
-  cfg.dynamicSmemBytes = 0;
-  cfg.stream = c.stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  void *rargs[1] = {&plan.r};
-  cudaError_t e = cudaLaunchKernelExC(&cfg, plan.fn, rargs);
-  if (e != cudaSuccess) {
-    cudaMemsetAsync(p.sched, 0, 2 * sizeof(int), c.stream);  // see above
-    return fail_cuda("launch reduce kernel", e);
-  }
-  return PA_OK;
+  st = launch_phase2(plan, c.stream);
+  if (st != PA_OK && phase1) cudaMemsetAsync(p.sched, 0, 2 * sizeof(int), c.stream);  // see above
+  return st;
+}
+
+// Phase 2 alone (pa_v2_combine): the partials are already in the workspace,
+// written by Phase 1 here or gathered from other GPUs.
+pa_status_t launch_combine(const Call &c) {
+  DeviceFacts *dev = nullptr;
+  pa_status_t st = device_facts(&dev);
+  if (st != PA_OK) return st;
+  const long long prows = (long long)c.num_seqs * c.num_heads;
+  if (prows == 0) return PA_OK;
+  size_t off[5];
+  if (pa_workspace_layout(c.num_seqs, c.num_heads, c.head_size, c.max_seq_len, c.partition_size,
+                          off) != PA_OK)
+    return PA_ERR_INVALID_ARG;
+  uint8_t *ws = static_cast<uint8_t *>(c.workspace);
+  AttnParams p;
+  memset(&p, 0, sizeof p);
+  p.status = reinterpret_cast<int *>(ws);
+  p.max_logits = reinterpret_cast<float *>(ws + off[1]);
+  p.exp_sums = reinterpret_cast<float *>(ws + off[2]);
+  p.tmp_out = reinterpret_cast<float *>(ws + off[3]);
+  const int mp = max_parts_of(c.max_seq_len, c.partition_size);
+  p.max_parts = mp > 0 ? mp : 1;
+  Phase2Plan plan;
+  st = plan_phase2(c, p, dev, prows, &plan);
+  if (st != PA_OK) return st;
+  return launch_phase2(plan, c.stream);
 }
 
 Call make_call(void *out, const void *query, const void *key_cache, const void *value_cache,
@@ -661,6 +733,41 @@ pa_status_t pa_forward(void *out, const void *query, const void *key_cache,
                        max_blocks_per_seq, max_seq_len, scale, partition_size, dtype, workspace,
                        workspace_bytes, stream),
              opt.variant, opt);
+}
+
+pa_status_t pa_v2_partials(const void *query, const void *key_cache, const void *value_cache,
+                           const int32_t *block_tables, const int32_t *seq_lens, int num_seqs,
+                           int num_heads, int num_kv_heads, int head_size, int num_blocks,
+                           int block_size, int max_blocks_per_seq, int max_seq_len, float scale,
+                           int partition_size, int dtype, int part_begin, int part_end,
+                           void *workspace, size_t workspace_bytes, void *stream) {
+  // `out` is never written in this mode; the query stands in for it in the
+  // argument checks (it has the same size and alignment rules).
+  Call c = make_call(const_cast<void *>(query), query, key_cache, value_cache, block_tables,
+                     seq_lens, num_seqs, num_heads, num_kv_heads, head_size, num_blocks,
+                     block_size, max_blocks_per_seq, max_seq_len, scale, partition_size, dtype,
+                     workspace, workspace_bytes, stream);
+  c.phases = 1;
+  c.part_begin = part_begin;
+  c.part_end = part_end;
+  pa_status_t st = check_args(c, true);
+  if (st != PA_OK) return st;
+  if (num_seqs == 0 || part_begin >= part_end) return PA_OK;
+  pa_options_t opt;
+  memset(&opt, 0, sizeof opt);
+  return launch(c, true, opt);
+}
+
+pa_status_t pa_v2_combine(void *out, const int32_t *seq_lens, int num_seqs, int num_heads,
+                          int head_size, int max_seq_len, int partition_size, int dtype,
+                          const void *workspace, size_t workspace_bytes, void *stream) {
+  Call c = make_call(out, nullptr, nullptr, nullptr, nullptr, seq_lens, num_seqs, num_heads, 1,
+                     head_size, 1, 16, 1, max_seq_len, 1.0f, partition_size, dtype,
+                     const_cast<void *>(workspace), workspace_bytes, stream);
+  c.phases = 2;
+  pa_status_t st = check_combine_args(c);
+  if (st != PA_OK) return st;
+  return launch_combine(c);
 }
 
 pa_status_t pa_chunks_forward(void *out, const void *query, const void *key_cache,

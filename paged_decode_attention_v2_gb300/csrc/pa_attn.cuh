@@ -622,8 +622,11 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) __maxnreg__((kernel_max_regs
       // sequence gets one item per KV head that writes zeros; lanes past the
       // last sequence count none.
       const int c_np = (c_L + p.range_tokens - 1) / p.range_tokens;
+      // V2 may be asked for a range of partitions only (context parallelism:
+      // the rest belong to other GPUs): [part_begin, part_end) of each sequence
+      const int c_nr = max(0, min(c_np, p.part_end) - p.part_begin);
       c_cnt = sl >= p.num_seqs ? 0
-                               : p.num_kv_heads * (c_np == 0 && p.fuse_limit > 0 ? 1 : c_np);
+                               : p.num_kv_heads * (c_np == 0 && p.fuse_limit > 0 ? 1 : c_nr);
       if constexpr (Math::kChunk) {
         // the sequence's query chunk: its last c_n tokens, query rows from c_qs;
         // items: (KV head, partition, group of chunk_tokens tokens)
@@ -717,9 +720,10 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) __maxnreg__((kernel_max_regs
               part = rem / nrg;
               rg = rem % nrg;
             } else {
-              const int items_per_head = np_s > 0 ? np_s : 1;
+              const int nr = max(0, min(np_s, p.part_end) - p.part_begin);
+              const int items_per_head = nr > 0 ? nr : 1;
               kvh = (item - first) / items_per_head;
-              part = (item - first) % items_per_head;
+              part = p.part_begin + (item - first) % items_per_head;
             }
             found = s < p.num_seqs;  // always, by the count above; never write past the batch
             break;

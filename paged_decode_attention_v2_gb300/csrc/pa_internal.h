@@ -33,6 +33,8 @@ struct AttnParams {
   int max_blocks_per_seq, max_seq_len, num_blocks;
   int range_tokens;   // tokens per work item: partition_size (V2) or max_seq_len (V1)
   int max_parts;      // partitions per (seq, head) in the workspace layout
+  int part_begin, part_end;  // V2: partitions [part_begin, part_end) of each
+                             // sequence only (0, INT_MAX: all of them)
   int write_partials; // 1: V2 Phase 1 outputs, 0: V1 final output
   int fuse_limit;     // V2: sequences of at most this many partitions get the
                       // cross-partition combine inside this kernel (0 = none)

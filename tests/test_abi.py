@@ -157,3 +157,61 @@ def test_host_staging_bytes(lib):
         12288 * 2 + 1280 + 256
     assert pa.pa_host_staging_bytes(-1, 8, 128, 10, pa.PA_DTYPE_BF16) == 0
     assert pa.pa_host_staging_bytes(3, 8, 128, 10, 7) == 0
+
+
+# ---- the split phases (context parallelism) --------------------------------
+
+def _partials(lib, part_begin, part_end, **over):
+    a = dict(query=FAKE, key_cache=FAKE, value_cache=FAKE, block_tables=FAKE, seq_lens=FAKE,
+             num_seqs=2, num_heads=8, num_kv_heads=2, head_size=128, num_blocks=64,
+             block_size=16, max_blocks_per_seq=8, max_seq_len=128, scale=0.1,
+             partition_size=512, dtype=pa.PA_DTYPE_BF16, workspace=FAKE,
+             workspace_bytes=1 << 30, stream=0)
+    a.update(over)
+    return lib.pa_v2_partials(a["query"], a["key_cache"], a["value_cache"], a["block_tables"],
+                              a["seq_lens"], a["num_seqs"], a["num_heads"], a["num_kv_heads"],
+                              a["head_size"], a["num_blocks"], a["block_size"],
+                              a["max_blocks_per_seq"], a["max_seq_len"], a["scale"],
+                              a["partition_size"], a["dtype"], part_begin, part_end,
+                              a["workspace"], a["workspace_bytes"], a["stream"])
+
+
+def _combine(lib, **over):
+    a = dict(out=FAKE, seq_lens=FAKE, num_seqs=2, num_heads=8, head_size=128, max_seq_len=128,
+             partition_size=512, dtype=pa.PA_DTYPE_BF16, workspace=FAKE,
+             workspace_bytes=1 << 30, stream=0)
+    a.update(over)
+    return lib.pa_v2_combine(a["out"], a["seq_lens"], a["num_seqs"], a["num_heads"],
+                             a["head_size"], a["max_seq_len"], a["partition_size"], a["dtype"],
+                             a["workspace"], a["workspace_bytes"], a["stream"])
+
+
+@pytest.mark.parametrize("rng,over,expect", [
+    ((-1, 4), {}, pa.PA_ERR_INVALID_ARG),             # negative start
+    ((3, 2), {}, pa.PA_ERR_INVALID_ARG),              # empty-backwards range
+    ((0, 1), dict(query=0), pa.PA_ERR_INVALID_ARG),
+    ((0, 1), dict(workspace=FAKE + 64), pa.PA_ERR_INVALID_ARG),
+    ((0, 1), dict(head_size=96), pa.PA_ERR_UNSUPPORTED),
+    ((0, 1), dict(workspace_bytes=pa.pa_workspace_bytes(2, 8, 128, 128, 512) - 1),
+     pa.PA_ERR_WORKSPACE_TOO_SMALL),
+    ((5, 5), {}, pa.PA_OK),                            # empty range: nothing to do
+    ((0, 4), dict(num_seqs=0), pa.PA_OK),              # no sequences: nothing to do
+])
+def test_partials_argument_errors(lib, rng, over, expect):
+    assert _partials(lib, *rng, **over) == expect
+
+
+@pytest.mark.parametrize("over,expect", [
+    (dict(out=0), pa.PA_ERR_INVALID_ARG),
+    (dict(seq_lens=0), pa.PA_ERR_INVALID_ARG),
+    (dict(out=FAKE + 4), pa.PA_ERR_INVALID_ARG),
+    (dict(workspace=FAKE + 16), pa.PA_ERR_INVALID_ARG),
+    (dict(head_size=96), pa.PA_ERR_UNSUPPORTED),
+    (dict(partition_size=100), pa.PA_ERR_UNSUPPORTED),
+    (dict(dtype=7), pa.PA_ERR_INVALID_ARG),
+    (dict(num_seqs=-1), pa.PA_ERR_INVALID_ARG),
+    (dict(workspace_bytes=pa.pa_workspace_bytes(2, 8, 128, 128, 512) - 1),
+     pa.PA_ERR_WORKSPACE_TOO_SMALL),
+])
+def test_combine_argument_errors(lib, over, expect):
+    assert _combine(lib, **over) == expect
