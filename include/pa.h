@@ -97,7 +97,11 @@ typedef struct {
 #define PA_DEBUG_STALL_CONSUMERS 1
 
 /* Bytes of workspace that pa_v2_forward needs (V1 needs only the 256-byte
- * status block).  Layout, each part 256-byte aligned, in this order:
+ * status block).  The partials are the three per-partition arrays that the
+ * "paged_attention_v2" commit note (project_6, commit 96f4baf "Dockerfile",
+ * section "Implementation", "Phase 1") has Phase 1 store for Phase 2:
+ * tmp_output, exp_sums and max_logits, kept in fp32 here.
+ * Layout, each part 256-byte aligned, in this order:
  *   status      int32 status word + work-queue counters (a 256-byte block)
  *   max_logits  f32 [num_seqs][num_heads][max_parts]   Phase 1 max logit
  *   exp_sums    f32 [num_seqs][num_heads][max_parts]   sum exp(logit - max)
@@ -122,9 +126,13 @@ pa_status_t pa_workspace_layout(int num_seqs, int num_heads, int head_size,
 pa_status_t pa_workspace_init(void *workspace, size_t workspace_bytes,
                               void *stream);
 
-/* V1: single pass over each whole sequence; one CTA per (sequence, KV head)
- * computing all num_heads/num_kv_heads query heads of the group with an
- * online softmax.  partition_size is validated but otherwise unused.
+/* V1: single pass over each whole sequence, the kernel the "paged_attention_v2"
+ * commit note (project_6, commit 96f4baf "Dockerfile") opens with: "V1
+ * limitation" describes it as one launch over the entire KV sequence, and its
+ * "Integration" list keeps it for sequences of up to 8192 tokens.  Here a
+ * work item is one (sequence, KV head), computing all num_heads/num_kv_heads
+ * query heads of the group with an online softmax; items are spread over a
+ * persistent grid.  partition_size is validated but otherwise unused.
  * The workspace needs >= 256 bytes (its status block). */
 pa_status_t pa_v1_forward(void *out, const void *query, const void *key_cache,
                           const void *value_cache, const int32_t *block_tables,
@@ -309,15 +317,23 @@ pa_status_t pa_v2_forward_noalloc(void *out, const void *query,
                                   int partition_size, int dtype, void *stream);
 
 /* Host heuristic: 1 if V2 should serve this batch on a GPU with sm_count
- * SMs, 0 for V1.  V1 when every sequence fits in one partition; otherwise V2
- * unless the batch alone fills the GPU several times over with short
- * sequences (the commit note's V1 range of seq_len <= 8192, scaled by how
- * many (sequence, KV head) CTAs there are per SM). */
+ * SMs, 0 for V1.  The pages switch on sequence length alone: the commit note
+ * for computility-run.yaml (project_6, commit a2a5dd8) lists the decode path
+ * as V1 up to 8192 tokens and V2 above, and GROUND_TRUTH_STATUS_v2.md
+ * (project_6_baseline5, section "路径 3") says the partitioning should follow
+ * the SM count.  Here: V1 when every sequence fits in one partition;
+ * otherwise V2 unless the batch alone fills the GPU several times over with
+ * short sequences (the length bound and the fill factor are set from
+ * measurements on GB300). */
 int pa_choose_v2(int num_seqs, int num_kv_heads, int max_seq_len,
                  int partition_size, int sm_count);
 
 /* Synchronise `stream`, return the workspace's status word as a pa_status_t
- * (PA_OK if no kernel reported a problem) and reset it to 0. */
+ * (PA_OK if no kernel reported a problem) and reset it to 0.  The pages have
+ * no counterpart: this is how the library reports data errors its kernels
+ * find (a block-table entry outside [0, num_blocks), a length outside
+ * [0, max_seq_len]) or a bounded device wait that ran out, since kernels
+ * never trap.  Not for use inside a stream capture (it synchronises). */
 pa_status_t pa_read_device_status(void *workspace, void *stream);
 
 /* Static English text for a status code. */

@@ -854,11 +854,25 @@ pa_status_t pa_forward_host(void *out_host, const void *query_host, const void *
 
 int pa_choose_v2(int num_seqs, int num_kv_heads, int max_seq_len, int partition_size,
                  int sm_count) {
+  // Every sequence in one partition: V2 would only add the reduce.
   if (partition_size < 1 || max_seq_len <= partition_size) return 0;
-  const long long v1_ctas = (long long)num_seqs * num_kv_heads;
-  // V1 only when its one-CTA-per-(sequence, KV head) grid already covers the
-  // GPU several times over and no sequence is long enough to unbalance it.
-  if (max_seq_len <= 8192 && sm_count > 0 && v1_ctas >= 8LL * sm_count) return 0;
+  if (sm_count <= 0) return 1;
+  // V1 has one work item per (sequence, KV head).  Measured on GB300 (bf16,
+  // D 128, 32 q / 4 kv heads, lengths uniform in [L/2, L], consecutive steps
+  // with the K/V cold in L2), V1 is ahead:
+  //   - with at least 16 items per SM, at every length (2-6 %): the items
+  //     balance over the persistent CTAs and V2's partials and reduce are
+  //     pure overhead;
+  //   - with 8 to 16 items per SM, up to 2 partitions of length;
+  //   - with 2 to 3 items per SM, i.e. one item per resident CTA with at
+  //     least two CTAs streaming on every SM, up to 4 partitions of length.
+  // Everywhere else (one CTA per SM, or a second round of uneven items)
+  // V2's finer items win.
+  const long long items = (long long)num_seqs * num_kv_heads;
+  const long long sm = sm_count;
+  if (items >= 16 * sm) return 0;
+  if (items >= 8 * sm && max_seq_len <= 2LL * partition_size) return 0;
+  if (items >= 2 * sm && items <= 3 * sm && max_seq_len <= 4LL * partition_size) return 0;
   return 1;
 }
 

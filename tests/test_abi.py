@@ -67,13 +67,39 @@ def test_workspace_layout_and_size(lib):
     assert pa.pa_workspace_bytes(1, 8, 64, 10, 0) == 0
 
 
+# The rule's cells as measured on GB300 (152 SMs, P = 512, 4 KV heads): the
+# V1/V2 sweep over (sequences x KV heads) in {1, 2, 4, 8, 16} x 152 and
+# max length in {512 .. 16384}.
+CHOOSE_V2_MEASURED = {
+    # (B*Hkv, max L): faster variant
+    (152, 512): 0, (152, 1024): 1, (152, 2048): 1, (152, 4096): 1, (152, 8192): 1,
+    (152, 16384): 1,
+    (304, 512): 0, (304, 1024): 0, (304, 2048): 0, (304, 4096): 1, (304, 8192): 1,
+    (304, 16384): 1,
+    (608, 512): 0, (608, 1024): 1, (608, 2048): 1, (608, 4096): 1, (608, 8192): 1,
+    (608, 16384): 1,
+    (1216, 512): 0, (1216, 1024): 0, (1216, 2048): 1, (1216, 4096): 1, (1216, 8192): 1,
+    (1216, 16384): 1,
+    (2432, 512): 0, (2432, 1024): 0, (2432, 2048): 0, (2432, 4096): 0, (2432, 8192): 0,
+    (2432, 16384): 0,
+}
+
+
+@pytest.mark.parametrize("cell", sorted(CHOOSE_V2_MEASURED))
+def test_choose_v2_matches_the_measured_crossover(lib, cell):
+    bh, L = cell
+    assert pa.pa_choose_v2(bh // 4, 4, L, 512, 152) == CHOOSE_V2_MEASURED[cell]
+
+
 @pytest.mark.parametrize("args,expect", [
     ((1, 4, 100000, 512, 152), 1),   # one long sequence: V2 spreads it over the GPU
-    ((8, 4, 8192, 512, 152), 1),     # few (seq, kv head) CTAs: V2
+    ((8, 4, 8192, 512, 152), 1),     # few (seq, kv head) items: V2
     ((64, 4, 512, 512, 152), 0),     # every sequence in one partition: V1
-    ((4096, 8, 4096, 512, 152), 0),  # 32K CTAs of short sequences: V1 fills the GPU
-    ((4096, 8, 20000, 512, 152), 1), # long sequences: V2
+    ((4096, 8, 4096, 512, 152), 0),  # 32K items of short sequences: V1 fills the GPU
+    ((4096, 8, 20000, 512, 152), 0), # 32K items: V1 balances at any length
+    ((256, 4, 3584, 512, 152), 1),   # 1024 items (6.7 per SM) of up to 7 partitions: V2
     ((1, 1, 0, 512, 152), 0),
+    ((76, 4, 1024, 512, 0), 1),      # unknown SM count: V2 unless one partition
 ])
 def test_choose_v2(lib, args, expect):
     assert pa.pa_choose_v2(*args) == expect
