@@ -263,16 +263,23 @@ size_t pa_host_staging_bytes(int num_seqs, int num_heads, int head_size,
  * workspace stay on the device.  `staging` is a caller-owned device buffer of
  * at least pa_host_staging_bytes(...) bytes, 256-byte aligned.
  *
- * Enqueues on `stream`, in order: one host-to-device copy each of seq_lens,
- * the block tables and the query into the staging buffer; the kernels of
- * pa_forward; one device-to-host copy of the output.  It returns when they
- * are enqueued: synchronise the stream before reading out_host.  Host
- * buffers in pinned memory let the copies run asynchronously; pageable ones
- * work too (the copies then synchronise the host with the stream).  The host
- * buffers and the staging buffer must stay untouched until the stream
- * reaches the end of the call.  Errors: as pa_forward, plus
- * PA_ERR_INVALID_ARG for a null host pointer or a staging buffer that is
- * null, misaligned or smaller than pa_host_staging_bytes(...). */
+ * When all four host buffers are pinned (page-locked, hence mapped into the
+ * device's address space; out_host 16-byte aligned), nothing goes through a
+ * copy engine: one kernel reads the lengths, block tables and queries from
+ * the host buffers into the staging buffer over the host link, and the last
+ * kernel of the forward stores the output straight into out_host.  Otherwise
+ * the call enqueues one host-to-device cudaMemcpyAsync each of seq_lens, the
+ * block tables and the query into the staging buffer, the kernels of
+ * pa_forward, and one device-to-host copy of the output (pageable buffers
+ * make those copies synchronise the host with the stream).
+ *
+ * Either way it returns when everything is enqueued on `stream`: synchronise
+ * the stream before reading out_host.  The host buffers and the staging
+ * buffer must stay untouched until the stream reaches the end of the call.
+ * Errors: as pa_forward, plus PA_ERR_INVALID_ARG for a null host pointer or
+ * a staging buffer that is null, misaligned or smaller than
+ * pa_host_staging_bytes(...); argument errors come back before anything is
+ * enqueued. */
 pa_status_t pa_forward_host(void *out_host, const void *query_host,
                             const void *key_cache, const void *value_cache,
                             const int32_t *block_tables_host,

@@ -651,6 +651,67 @@ pa_status_t run(const Call &c, int variant, const pa_options_t &opt) {
   return launch(c, v2, opt);
 }
 
+// The device-side address of host memory, if it is pinned (page-locked and
+// mapped into the current device's address space); false for pageable
+// memory, which only the copy engines may read.
+bool device_view(const void *host, const void **dev) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, host) != cudaSuccess) {
+    cudaGetLastError();  // clear the sticky-free error of an unknown pointer
+    return false;
+  }
+  if (a.type != cudaMemoryTypeHost || !a.devicePointer) return false;
+  *dev = a.devicePointer;
+  return true;
+}
+bool device_view(void *host, void **dev) {
+  const void *d = nullptr;
+  if (!device_view(static_cast<const void *>(host), &d)) return false;
+  *dev = const_cast<void *>(d);
+  return true;
+}
+
+// Enqueue the kernel that copies pa_forward_host's inputs (three segments:
+// lengths, block tables, queries) from mapped host memory into staging.
+pa_status_t stage_in(const void *s0, void *d0, size_t b0, const void *s1, void *d1, size_t b1,
+                     const void *s2, void *d2, size_t b2, cudaStream_t stream) {
+  DeviceFacts *dev = nullptr;
+  pa_status_t st = device_facts(&dev);
+  if (st != PA_OK) return st;
+  StageInParams p;
+  memset(&p, 0, sizeof p);
+  const void *src[3] = {s0, s1, s2};
+  void *dst[3] = {d0, d1, d2};
+  const size_t bytes[3] = {b0, b1, b2};
+  long long units16 = 0;
+  for (int i = 0; i < kStageInSegments; ++i) {
+    const bool wide = aligned(src[i], 16) && aligned(dst[i], 16) && bytes[i] % 16 == 0;
+    p.src[i] = src[i];
+    p.dst[i] = dst[i];
+    p.width[i] = wide ? 16 : 4;  // every segment is a whole number of 4-byte words
+    p.units[i] = (long long)(bytes[i] / p.width[i]);
+    units16 += (long long)((bytes[i] + 15) / 16);
+  }
+  // about four 16-byte units per thread, at most four CTAs per SM
+  long long ctas = (units16 + 4 * 256 - 1) / (4 * 256);
+  if (ctas > 4LL * dev->sm_count) ctas = 4LL * dev->sm_count;
+  if (ctas < 1) ctas = 1;
+  cudaLaunchConfig_t cfg;
+  memset(&cfg, 0, sizeof cfg);
+  cfg.gridDim = dim3((unsigned)ctas, 1, 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  void *args[1] = {&p};
+  cudaError_t e = cudaLaunchKernelExC(&cfg, stage_in_kernel(), args);
+  if (e != cudaSuccess) return fail_cuda("launch stage-in kernel", e);
+  return PA_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -828,16 +889,30 @@ pa_status_t pa_forward_host(void *out_host, const void *query_host, const void *
   void *out_dev = st + align256(qbytes);
   int32_t *bt_dev = reinterpret_cast<int32_t *>(st + 2 * align256(qbytes));
   int32_t *sl_dev = reinterpret_cast<int32_t *>(st + 2 * align256(qbytes) + align256(tbytes));
-  const Call c = make_call(out_dev, q_dev, key_cache, value_cache, bt_dev, sl_dev, num_seqs,
-                           num_heads, num_kv_heads, head_size, num_blocks, block_size,
-                           max_blocks_per_seq, max_seq_len, scale, partition_size, dtype,
-                           workspace, workspace_bytes, stream);
+  Call c = make_call(out_dev, q_dev, key_cache, value_cache, bt_dev, sl_dev, num_seqs,
+                     num_heads, num_kv_heads, head_size, num_blocks, block_size,
+                     max_blocks_per_seq, max_seq_len, scale, partition_size, dtype, workspace,
+                     workspace_bytes, stream);
+  // Pinned host buffers are mapped into the device: then a kernel reads the
+  // inputs and the last kernel writes the output in place (no copy engine).
+  void *out_map = nullptr;
+  const void *q_map = nullptr, *bt_map = nullptr, *sl_map = nullptr;
+  const bool mapped = device_view(out_host, &out_map) && device_view(query_host, &q_map) &&
+                      device_view(block_tables_host, &bt_map) &&
+                      device_view(seq_lens_host, &sl_map) && aligned(out_map, 16);
+  if (mapped) c.out = out_map;
   // argument problems are reported before anything is enqueued
   bool v2 = false;
   pa_status_t chk = resolve(c, opt.variant, &v2);
   if (chk != PA_OK) return chk;
   if (num_seqs == 0) return PA_OK;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (mapped) {
+    pa_status_t r = stage_in(sl_map, sl_dev, (size_t)num_seqs * 4, bt_map, bt_dev, tbytes, q_map,
+                             q_dev, qbytes, s);
+    if (r != PA_OK) return r;
+    return launch(c, v2, opt);
+  }
   cudaError_t e = cudaMemcpyAsync(sl_dev, seq_lens_host, (size_t)num_seqs * 4,
                                   cudaMemcpyHostToDevice, s);
   if (e != cudaSuccess) return fail_cuda("cudaMemcpyAsync(seq_lens)", e);

@@ -986,11 +986,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) __maxnreg__((kernel_max_regs
             p.exp_sums[row] = ml.y;
           }
         } else {
-          T *o = static_cast<T *>(p.out) + orow * D + d;
-          o[0] = from_float<T>(acc.x);
-          o[1] = from_float<T>(acc.y);
-          o[2] = from_float<T>(acc.z);
-          o[3] = from_float<T>(acc.w);
+          store4(static_cast<T *>(p.out) + orow * D + d, acc.x, acc.y, acc.z, acc.w);
         }
       }
       if (!Math::kChunk && p.write_partials && h.np <= p.fuse_limit) {
@@ -1057,11 +1053,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) __maxnreg__((kernel_max_regs
                 acc.w = fmaf(w, v[u].w, acc.w);
               }
             }
-            T *o = static_cast<T *>(p.out) + (head0 + hh) * D + d;
-            o[0] = from_float<T>(acc.x);
-            o[1] = from_float<T>(acc.y);
-            o[2] = from_float<T>(acc.z);
-            o[3] = from_float<T>(acc.w);
+            store4(static_cast<T *>(p.out) + (head0 + hh) * D + d, acc.x, acc.y, acc.z, acc.w);
           }
           if (threadIdx.x == 0) *cnt = 0;  // ready for the next launch
         }

@@ -259,6 +259,24 @@ __device__ __forceinline__ __nv_bfloat16 from_float<__nv_bfloat16>(float x) {
 template <>
 __device__ __forceinline__ __half from_float<__half>(float x) { return __float2half_rn(x); }
 
+// Round four floats to T (nearest even, as from_float) and store them with one
+// 16-byte (float) or 8-byte (16-bit) store; `o` is aligned to four elements.
+// One wide store instead of four narrow ones also suits outputs that live in
+// host memory mapped into the device (pa_forward_host).
+__device__ __forceinline__ void store4(float *o, float a, float b, float c, float d) {
+  *reinterpret_cast<float4 *>(o) = make_float4(a, b, c, d);
+}
+__device__ __forceinline__ void store4(__nv_bfloat16 *o, float a, float b, float c, float d) {
+  const __nv_bfloat162 lo = __floats2bfloat162_rn(a, b), hi = __floats2bfloat162_rn(c, d);
+  *reinterpret_cast<uint2 *>(o) = make_uint2(*reinterpret_cast<const uint32_t *>(&lo),
+                                             *reinterpret_cast<const uint32_t *>(&hi));
+}
+__device__ __forceinline__ void store4(__half *o, float a, float b, float c, float d) {
+  const __half2 lo = __floats2half2_rn(a, b), hi = __floats2half2_rn(c, d);
+  *reinterpret_cast<uint2 *>(o) = make_uint2(*reinterpret_cast<const uint32_t *>(&lo),
+                                             *reinterpret_cast<const uint32_t *>(&hi));
+}
+
 // Widen the 16 bytes of one shared-memory chunk to floats: 4 (f32) or 8 (16-bit).
 __device__ __forceinline__ void chunk_to_float(const uint4 &c, float (&f)[4]) {
   f[0] = __uint_as_float(c.x);

@@ -69,6 +69,17 @@ struct ReduceParams {
   int *sched;          // non-null: Phase 1's work counters, zeroed after the wait
 };
 
+// Parameters of the kernel that reads pa_forward_host's inputs from pinned
+// host memory: segment i is units[i] elements of width[i] bytes (16 or 4)
+// from src[i] (a device-side address of host memory) to dst[i] (staging).
+constexpr int kStageInSegments = 3;
+struct StageInParams {
+  const void *src[kStageInSegments];
+  void *dst[kStageInSegments];
+  long long units[kStageInSegments];
+  int width[kStageInSegments];
+};
+
 enum MathKind { kMathSimt = 1, kMathTensor = 2 };
 
 // Static description of one compiled attention kernel.
@@ -109,5 +120,6 @@ AttnKernelInfo attn_kernel_simt_f16(int head_size, int group);
 AttnKernelInfo attn_kernel_chunk_bf16(int head_size);
 AttnKernelInfo attn_kernel_chunk_f16(int head_size);
 const void *reduce_kernel(int dtype, int float4_per_thread);
+const void *stage_in_kernel();
 
 }  // namespace pa

@@ -217,11 +217,8 @@ __global__ void __launch_bounds__(kReduceThreads, 4)
       const float inv = np > 0 ? 1.f / acc.S : 0.f;  // np == 0: empty sequence -> zeros
 #pragma unroll
       for (int k = 0; k < VPT; ++k) {
-        OutT *o = out + 4 * (cl + C * k);
-        o[0] = from_float<OutT>(acc.a[k].x * inv);
-        o[1] = from_float<OutT>(acc.a[k].y * inv);
-        o[2] = from_float<OutT>(acc.a[k].z * inv);
-        o[3] = from_float<OutT>(acc.a[k].w * inv);
+        store4(out + 4 * (cl + C * k), acc.a[k].x * inv, acc.a[k].y * inv, acc.a[k].z * inv,
+               acc.a[k].w * inv);
       }
     }
     if (W > 1) team_sync(g, W * 32);  // the shared slots are free for the next task

@@ -5,8 +5,9 @@ Its scratch is the library's own fixed device array, so the caller passes
 only inputs and outputs.
 
 Called here straight through the C ABI (ctypes), twice in a row, and compared
-with the ordinary pa_v2_forward (caller-owned workspace) at the tests' bf16
-tolerance.  This file sorts last so that a run stopping at the first failure
+on each call both with the ordinary pa_v2_forward (caller-owned workspace)
+and with the CPU fp64 oracle, at the tests' bf16 tolerance: the second
+comparison would also catch a fault shared by the two entry points' kernels.  This file sorts last so that a run stopping at the first failure
 has run every other test before it; it also passes on its own in a fresh
 process.
 """
@@ -17,7 +18,7 @@ import torch
 
 import paged_decode_attention_v2_gb300 as pa
 import workloads
-from gpu_helpers import DeviceCase, assert_close
+from gpu_helpers import DeviceCase, assert_close, reference
 
 pytestmark = pytest.mark.gpu
 
@@ -44,11 +45,13 @@ def test_noalloc_matches_the_workspace_entry_point_twice():
                      max_seq_len=dc.max_seq_len)
     assert pa.pa_read_device_status(dc.ws) == pa.PA_OK
     ref_np = ref.double().cpu().numpy()
+    exact = reference(case)
     for _ in range(2):
         out = torch.full_like(dc.q, float("nan"))
         assert _noalloc(lib, dc, out) == pa.PA_OK
         torch.cuda.synchronize()
         assert_close(out, ref_np, torch.bfloat16, "noalloc vs pa_v2_forward")
+        assert_close(out, exact, torch.bfloat16, "noalloc vs the fp64 oracle")
 
 
 def test_noalloc_refuses_requests_beyond_its_scratch():
