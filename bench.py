@@ -58,6 +58,7 @@ UNIT = "GB/s"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 CHUNK_TOKENS = 4
+LONG_CHUNK_TOKENS = 64
 MAX_LAYERS = 64
 # the other workloads reported beside the headline, each timed like it
 SECONDARY = [("c3_long_100k", None), ("c2_gqa_batch8", None), ("c5_mixed_d256", 512),
@@ -378,7 +379,7 @@ class ChunkRunner:
         self.pa.pa_chunks_forward(out, q, kc, vc, self.bt, self.sl,
                                   self.q_start, self.case.scale, self.case.partition_size,
                                   self.ws, max_seq_len=self.case.max_seq_len,
-                                  max_chunk=self.tokens)
+                                  max_chunk=self.tokens, phase1_event=phase1_event)
 
     def check_status(self):
         st = self.pa.pa_read_device_status(self.ws)
@@ -749,6 +750,22 @@ def run_ours(args):
         ce["query_rows_per_s"] = round(cr.q.shape[0] / (ce["ms_per_step"] / 1e3), 1)
         ce.pop("tokens_per_s", None)
         line["chunks"] = ce
+        del cr
+        torch.cuda.empty_cache()
+        # long chunks (a prefill chunk whose keys and values are already cached):
+        # 64 tokens per sequence, 512 (token, head) rows per KV head
+        cr = ChunkRunner(case, device, LONG_CHUNK_TOKENS,
+                         layers=max(1, layers_for(case.kv_bytes(), l2)))
+        ce = measure(args.workload, case, cr, flush, peak, 20, 20)
+        ce["workload"] = f"{args.workload}, {LONG_CHUNK_TOKENS}-token query chunks"
+        ce["query_rows_per_s"] = round(cr.q.shape[0] / (ce["ms_per_step"] / 1e3), 1)
+        ce.pop("tokens_per_s", None)
+        rows = cr.q.shape[0] * case.num_heads
+        vis = float(case.seq_lens.double().sum()) - case.num_seqs * (LONG_CHUNK_TOKENS - 1) / 2
+        flops = 4.0 * case.num_heads * LONG_CHUNK_TOKENS * vis * case.head_size
+        ce["attention_tflops"] = round(flops / (ce["ms_per_step"] / 1e3) / 1e12, 1)
+        ce["rows"] = rows
+        line["long_chunks"] = ce
         del cr
         torch.cuda.empty_cache()
     if world == 1 and not args.no_cpu_baseline and not args.no_secondary:

@@ -249,20 +249,25 @@ def pa_v2_forward_noalloc(out, query, key_cache, value_cache, block_tables, seq_
            "pa_v2_forward_noalloc")
 
 
+def _event_handle(ev):
+    """The cudaEvent_t of a torch.cuda.Event (or a raw handle), or None."""
+    if ev is None:
+        return None
+    h = ev.cuda_event if hasattr(ev, "cuda_event") else int(ev)
+    if not h:
+        raise ValueError("phase1_event has no CUDA event yet (torch creates it at the "
+                         "first record(); record it once before passing it)")
+    return h
+
+
 def pa_forward(out, query, key_cache, value_cache, block_tables, seq_lens, scale,
                partition_size, workspace, max_seq_len=None, stream=None, variant=PA_VARIANT_AUTO,
                math=PA_MATH_AUTO, num_stages=0, debug_flags=0, wait_limit_ns=0,
                phase1_event=None, ctas_per_sm=0, fuse_partitions=0) -> None:
     """V1 or V2 chosen by pa_choose_v2, or forced through the options.
     ``phase1_event`` (a torch.cuda.Event) is recorded between V2's two kernels."""
-    ev = 0
-    if phase1_event is not None:
-        ev = phase1_event.cuda_event if hasattr(phase1_event, "cuda_event") else int(phase1_event)
-        if not ev:
-            raise ValueError("phase1_event has no CUDA event yet (torch creates it at the "
-                             "first record(); record it once before passing it)")
-    opts = pa_options_t(variant, math, num_stages, debug_flags, wait_limit_ns, ev, ctas_per_sm,
-                        fuse_partitions)
+    opts = pa_options_t(variant, math, num_stages, debug_flags, wait_limit_ns,
+                        _event_handle(phase1_event), ctas_per_sm, fuse_partitions)
     _check(load_library().pa_forward(*_fwd_args(
         out, query, key_cache, value_cache, block_tables, seq_lens, scale, partition_size,
         workspace, max_seq_len, stream), ctypes.byref(opts)), "pa_forward")
@@ -270,7 +275,8 @@ def pa_forward(out, query, key_cache, value_cache, block_tables, seq_lens, scale
 
 def pa_chunks_forward(out, query, key_cache, value_cache, block_tables, seq_lens, q_start,
                       scale, partition_size, workspace, max_seq_len=None, max_chunk=None,
-                      stream=None, variant=PA_VARIANT_AUTO, num_stages=0, ctas_per_sm=0) -> None:
+                      stream=None, variant=PA_VARIANT_AUTO, num_stages=0, ctas_per_sm=0,
+                      phase1_event=None) -> None:
     """Multi-token queries over the paged cache (see include/pa.h): query and
     out [num_rows, H, D]; the chunk of sequence s is rows q_start[s] ..
     q_start[s+1]-1 (int32 on the device), its last tokens.  max_chunk bounds
@@ -285,7 +291,8 @@ def pa_chunks_forward(out, query, key_cache, value_cache, block_tables, seq_lens
     if max_seq_len is None:
         max_seq_len = block_tables.shape[1] * bs
     mc = int(max_chunk) if max_chunk is not None else int(max_seq_len)
-    opts = pa_options_t(variant, PA_MATH_AUTO, num_stages, 0, 0, None, ctas_per_sm, 0)
+    opts = pa_options_t(variant, PA_MATH_AUTO, num_stages, 0, 0, _event_handle(phase1_event),
+                        ctas_per_sm, 0)
     _check(load_library().pa_chunks_forward(
         _ptr(out), _ptr(query), _ptr(key_cache), _ptr(value_cache), _ptr(block_tables),
         _ptr(seq_lens), _ptr(q_start), B, R, mc, H, hkv, D, nb, bs, block_tables.shape[1],

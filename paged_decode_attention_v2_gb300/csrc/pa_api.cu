@@ -404,8 +404,9 @@ pa_status_t launch(const Call &c, bool v2, const pa_options_t &opt) {
   const bool chunk = c.q_start != nullptr;
   if (chunk && math != kMathTensor) return PA_ERR_UNSUPPORTED;
   const AttnKernelInfo k =
-      chunk ? (c.dtype == PA_DTYPE_BF16 ? attn_kernel_chunk_bf16(c.head_size)
-                                        : attn_kernel_chunk_f16(c.head_size))
+      chunk ? (c.dtype == PA_DTYPE_BF16
+                   ? attn_kernel_chunk_bf16(c.head_size, group, c.max_chunk * group)
+                   : attn_kernel_chunk_f16(c.head_size, group, c.max_chunk * group))
             : pick_kernel(math, c.dtype, c.head_size, group);
   if (!k.fn) return PA_ERR_UNSUPPORTED;
 
@@ -423,7 +424,8 @@ pa_status_t launch(const Call &c, bool v2, const pa_options_t &opt) {
   if (stages == 0) {
     long long best = 0;
     for (int n = 2; n <= 8; ++n) {
-      const size_t b = attn_smem_bytes(c.head_size, elt, k.consumer_warps, k.max_group, n, simt);
+      const size_t b = attn_smem_bytes(c.head_size, elt, k.stage_tokens, k.consumer_warps,
+                                       k.max_group, n, simt);
       if (b > (size_t)dev->max_smem_optin) break;
       st = ensure_smem(k.fn, b);
       if (st != PA_OK) return st;
@@ -438,7 +440,8 @@ pa_status_t launch(const Call &c, bool v2, const pa_options_t &opt) {
     }
     if (stages <= 0) return PA_ERR_UNSUPPORTED;
   }
-  size_t smem = attn_smem_bytes(c.head_size, elt, k.consumer_warps, k.max_group, stages, simt);
+  size_t smem = attn_smem_bytes(c.head_size, elt, k.stage_tokens, k.consumer_warps, k.max_group,
+                                stages, simt);
   if (smem > (size_t)dev->max_smem_optin) return PA_ERR_UNSUPPORTED;
 
   const int unit_rows = c.block_size < k.stage_tokens ? c.block_size : k.stage_tokens;
@@ -505,7 +508,7 @@ pa_status_t launch(const Call &c, bool v2, const pa_options_t &opt) {
   if (chunk) {
     p.q_start = c.q_start;
     p.num_rows = c.num_rows;
-    p.chunk_tokens = chunk_tokens_of(c);
+    p.chunk_tokens = k.max_group / group;  // tokens of an item: its rows / heads per token
   }
   p.num_stages = stages;
   p.debug_flags = opt.debug_flags;

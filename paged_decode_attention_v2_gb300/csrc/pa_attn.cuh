@@ -103,6 +103,7 @@ struct TensorMath {
   // Query chunks (several tokens of a sequence per item, causal among them):
   // the columns are (token, head) rows, each with its own key limit.
   static constexpr bool kChunk = CHUNK;
+  static constexpr bool kRowOwning = false;
   uint32_t qf[NT][KS][2];
   float o[NT][KS][4];
   float m[NT][2];
@@ -308,6 +309,212 @@ struct TensorMath {
   }
 };
 
+
+// ---------------------------------------------------------------------------
+// Query chunks with row-owning warps (bf16 / f16, D 64 or 128).  An item is
+// up to 16 x NWC of the chunk's (token, head) rows; consumer warp w owns rows
+// [16 w, 16 w + 16) of it and runs them over every key of each 64-key stage:
+//   S[16 rows][64 keys] = Q[16][D] . K^T              (mma m16n8k16, A = Q)
+//   O[16 rows][D]      += P[16][64 keys] . V[64][D]    (A = P, taken straight
+//                                                       from S's accumulators)
+// A row's statistics live in the four lanes of a quad, and no warp holds
+// another's rows, so an item ends without a cross-warp merge: each warp
+// writes its rows from registers, and the stage goes back to the producer as
+// soon as its tile is done.  Each warp's tile carries 8 (S) and 16 (O)
+// independent accumulator chains.  Accumulation is fp32; P is rounded to the
+// input type for the PV product and the row sum adds the rounded values.
+template <typename T, int D, int NWC>
+struct RowMath {
+  static constexpr bool kChunk = true;
+  static constexpr bool kRowOwning = true;
+  static constexpr int ST = 64;          // keys per stage
+  static constexpr int KS = D / 16;      // k-steps of S = Q K^T
+  static constexpr int NK = ST / 8;      // key n-tiles of S
+  static constexpr int ND = D / 8;       // d n-tiles of O
+  static constexpr int KK = ST / 16;     // key k-steps of O += P V
+  static constexpr int GMAX = 16 * NWC;  // rows of an item
+  uint32_t qa[KS][4];  // A fragments of this warp's 16 query rows
+  float o[ND][4];
+  float m[2], l[2];    // rows r0 = lane / 4 and r0 + 8 of the warp: running max (log2), sum
+  int lim[2];          // keys at or past lim[i] are hidden from row i (0: not a row of the item)
+
+  // Start an item: rows [0, rows) of the q slot (row-major [GMAX][D], input
+  // type) are the item's; row r is the (r / group)-th token's head r % group,
+  // which sees the keys below lim_base + r / group + 1.
+  __device__ __forceinline__ void begin_item(const uint8_t *q_smem, int rows, int lane, int warp,
+                                             int lim_base, int group) {
+    // ldmatrix.x4 per k-step: lanes 0-15 give rows 0-15 at the k-step's first
+    // 8 columns, lanes 16-31 the same rows at its last 8 (A layout a0..a3)
+    const uint32_t a_row = smem_u32(q_smem) + (uint32_t)(16 * warp + (lane & 15)) * (D * sizeof(T)) +
+                           (uint32_t)(lane >> 4) * 16u;
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks)
+      ldsm_x4(a_row + (uint32_t)ks * 32u, qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3]);
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int r = 16 * warp + (lane >> 2) + 8 * i;
+      lim[i] = r < rows ? lim_base + r / group + 1 : 0;
+      m[i] = -CUDART_INF_F;
+      l[i] = 0.f;
+    }
+#pragma unroll
+    for (int d = 0; d < ND; ++d)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) o[d][j] = 0.f;
+  }
+
+  // One stage: keys [abs0, abs0 + valid) of the item, at positions 0.. of
+  // the stage buffers.
+  __device__ __forceinline__ void tile(uint32_t kbase, uint32_t vbase, const StageGeom &g, int,
+                                       int valid, int lane, float scale_log2, int abs0) {
+    const int mi = lane >> 3, r = lane & 7, q4 = lane & 3;
+    // ---- S = Q K^T: matrix mi of an ldmatrix.x4 is keys 16 jp + r + 8 (mi >> 1)
+    // at the k-step's 16-byte chunk 2 ks + (mi & 1): the B fragments of key
+    // n-tiles 2 jp and 2 jp + 1
+    float s[NK][4];
+#pragma unroll
+    for (int j = 0; j < NK; ++j)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) s[j][e] = 0.f;
+    {
+      uint32_t krow[NK / 2];
+      int ktok[NK / 2];
+#pragma unroll
+      for (int jp = 0; jp < NK / 2; ++jp) {
+        ktok[jp] = 16 * jp + r + ((mi >> 1) << 3);
+        krow[jp] = g.row_addr(kbase, ktok[jp]);
+      }
+#pragma unroll
+      for (int ks = 0; ks < KS; ++ks)
+#pragma unroll
+        for (int jp = 0; jp < NK / 2; ++jp) {
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4(g.chunk_addr(krow[jp], ktok[jp], 2 * ks + (mi & 1)), b0, b1, b2, b3);
+          MmaOp<T>::run(s[2 * jp], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1);
+          MmaOp<T>::run(s[2 * jp + 1], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b2, b3);
+        }
+    }
+    // ---- online softmax per row (log2 domain); hidden keys get -inf
+    float mx0 = -CUDART_INF_F, mx1 = -CUDART_INF_F;
+#pragma unroll
+    for (int j = 0; j < NK; ++j)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int kr = 8 * j + 2 * q4 + (e & 1);  // key within the stage
+        float x = s[j][e] * scale_log2;
+        if (kr >= valid || abs0 + kr >= lim[e >> 1]) x = -CUDART_INF_F;
+        s[j][e] = x;
+        if (e < 2)
+          mx0 = fmaxf(mx0, x);
+        else
+          mx1 = fmaxf(mx1, x);
+      }
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+    const float mn0 = fmaxf(m[0], mx0), mn1 = fmaxf(m[1], mx1);
+    // a row that has seen no key yet keeps m = -inf: its exponents are taken
+    // against 0 so that they come out 0, not NaN
+    const float mb0 = mn0 == -CUDART_INF_F ? 0.f : mn0;
+    const float mb1 = mn1 == -CUDART_INF_F ? 0.f : mn1;
+    const float al0 = exp2f(m[0] - mb0), al1 = exp2f(m[1] - mb1);
+    // P as the A fragments of the PV product: k-step kk takes key n-tiles
+    // 2 kk (a0: row r0, a1: row r0 + 8) and 2 kk + 1 (a2, a3)
+    uint32_t pa[KK][4];
+    float ls0 = 0.f, ls1 = 0.f;
+#pragma unroll
+    for (int kk = 0; kk < KK; ++kk)
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        const int j = 2 * kk + hf;
+        const uint32_t lo = MmaOp<T>::pack(exp2f(s[j][0] - mb0), exp2f(s[j][1] - mb0));
+        const uint32_t hi = MmaOp<T>::pack(exp2f(s[j][2] - mb1), exp2f(s[j][3] - mb1));
+        const float2 fl = MmaOp<T>::unpack(lo), fh = MmaOp<T>::unpack(hi);
+        ls0 += fl.x + fl.y;
+        ls1 += fh.x + fh.y;
+        pa[kk][2 * hf] = lo;
+        pa[kk][2 * hf + 1] = hi;
+      }
+    l[0] = l[0] * al0 + ls0;
+    l[1] = l[1] * al1 + ls1;
+    m[0] = mn0;
+    m[1] = mn1;
+    if (al0 != 1.f || al1 != 1.f) {
+#pragma unroll
+      for (int d = 0; d < ND; ++d) {
+        o[d][0] *= al0;
+        o[d][1] *= al0;
+        o[d][2] *= al1;
+        o[d][3] *= al1;
+      }
+    }
+    // ---- O += P V: matrix mi of an ldmatrix.x4.trans is keys 16 kk + r +
+    // 8 (mi & 1) at d chunk 2 jd + (mi >> 1): the B fragments of d n-tiles
+    // 2 jd and 2 jd + 1.  Keys past `valid` may hold stale bytes (NaN x 0
+    // would reach O): their V halves are cleared in the fragments.
+    const int k0 = 2 * q4;
+#pragma unroll
+    for (int kk = 0; kk < KK; ++kk) {
+      const int tk = 16 * kk + r + ((mi & 1) << 3);
+      const uint32_t vrow = g.row_addr(vbase, tk);
+      uint32_t keep_lo = 0xffffffffu, keep_hi = 0xffffffffu;  // keys 16 kk + k0 (+1), and + 8
+      if (valid < ST) {
+        const int a = 16 * kk + k0;
+        keep_lo = (a < valid ? 0x0000ffffu : 0u) | (a + 1 < valid ? 0xffff0000u : 0u);
+        keep_hi = (a + 8 < valid ? 0x0000ffffu : 0u) | (a + 9 < valid ? 0xffff0000u : 0u);
+      }
+#pragma unroll
+      for (int jd = 0; jd < ND / 2; ++jd) {
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4_trans(g.chunk_addr(vrow, tk, 2 * jd + (mi >> 1)), b0, b1, b2, b3);
+        b0 &= keep_lo;
+        b2 &= keep_lo;
+        b1 &= keep_hi;
+        b3 &= keep_hi;
+        MmaOp<T>::run(o[2 * jd], pa[kk][0], pa[kk][1], pa[kk][2], pa[kk][3], b0, b1);
+        MmaOp<T>::run(o[2 * jd + 1], pa[kk][0], pa[kk][1], pa[kk][2], pa[kk][3], b2, b3);
+      }
+    }
+  }
+
+  // End of an item: this warp's rows from registers.  V2 writes the
+  // partition's max logit (natural-log units), exp-sum and normalised output
+  // row; V1 the output rows.  Rows of the item start at query row row0; row
+  // r is token r / group, head kvh * group + r % group.
+  __device__ __forceinline__ void finish(const AttnParams &p, int row0, int kvh, int part,
+                                         int rows, int lane, int warp) const {
+    const int q4 = lane & 3;
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      float lt = l[i];
+      lt += __shfl_xor_sync(0xffffffffu, lt, 1);
+      lt += __shfl_xor_sync(0xffffffffu, lt, 2);
+      const int r = 16 * warp + (lane >> 2) + 8 * i;
+      if (r >= rows) continue;
+      const size_t orow = ((size_t)row0 + r / p.group) * p.num_heads + (size_t)kvh * p.group +
+                          r % p.group;
+      const float inv = lt > 0.f ? 1.f / lt : 0.f;
+      if (p.write_partials) {
+        const size_t prow = orow * p.max_parts + part;
+        float *dst = p.tmp_out + prow * D + 2 * q4;
+#pragma unroll
+        for (int d = 0; d < ND; ++d)
+          *reinterpret_cast<float2 *>(dst + 8 * d) = make_float2(o[d][2 * i] * inv, o[d][2 * i + 1] * inv);
+        if (q4 == 0) {
+          p.max_logits[prow] = m[i] * 0.69314718055994530942f;  // back to natural-log units
+          p.exp_sums[prow] = lt;
+        }
+      } else {
+        T *dst = static_cast<T *>(p.out) + orow * D + 2 * q4;
+#pragma unroll
+        for (int d = 0; d < ND; ++d)
+          *reinterpret_cast<uint32_t *>(dst + 8 * d) = MmaOp<T>::pack(o[d][2 * i] * inv, o[d][2 * i + 1] * inv);
+      }
+    }
+  }
+};
+
 // ---------------------------------------------------------------------------
 // CUDA-core fp32 math (any element type; the only path for f32).  Lane
 // (tok = lane % 16, half = lane / 16) forms the dot products of one token
@@ -317,6 +524,7 @@ struct TensorMath {
 template <typename T, int D, int GMAX>
 struct SimtMath {
   static constexpr bool kChunk = false;  // query chunks run on the tensor path only
+  static constexpr bool kRowOwning = false;
   static constexpr int ELT = sizeof(T);
   static constexpr int CPR = D * ELT / 16;  // 16-byte chunks per row
   static constexpr int EPC = 16 / ELT;      // elements per chunk
@@ -513,13 +721,30 @@ constexpr int kernel_max_regs() {
   return GMAX > 8 ? (NW == 4 ? 168 : 255) : (NW == 4 ? 128 : (NW == 2 ? 168 : 255));
 }
 
+// Row-owning query chunks: two CTAs per SM (their shared memory allows no
+// more), so with 4 consumer warps (5 warps a CTA) up to 204 registers fit.
+template <class Math, int NW, int GMAX>
+constexpr int attn_max_regs() {
+  return Math::kRowOwning ? (NW == 4 ? 200 : 255) : kernel_max_regs<NW, GMAX>();
+}
+
+// Tokens of one ring stage: 16 per consumer warp, or 64 for row-owning warps
+// (which each run every key of the stage).
+template <class Math, int NW>
+constexpr int stage_tokens() {
+  if constexpr (Math::kRowOwning)
+    return Math::ST;
+  else
+    return NW * kTileTokens;
+}
+
 // ---------------------------------------------------------------------------
 template <typename T, int D, int NW, int GMAX, class Math, bool SIMT>
-__global__ void __launch_bounds__((NW + 1) * 32, 1) __maxnreg__((kernel_max_regs<NW, GMAX>()))
+__global__ void __launch_bounds__((NW + 1) * 32, 1) __maxnreg__((attn_max_regs<Math, NW, GMAX>()))
     pa_attn_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CUtensorMap tmap_k,
                    const __grid_constant__ CUtensorMap tmap_v) {
   constexpr int ELT = sizeof(T);
-  constexpr int ST = NW * kTileTokens;  // tokens per stage
+  constexpr int ST = stage_tokens<Math, NW>();  // tokens per stage
   constexpr int ROW_BYTES = D * ELT;
   constexpr int NPANELS = ROW_BYTES / kPanelBytes;
   constexpr int HALF_BYTES = ST * ROW_BYTES;  // K (or V) bytes of one stage
@@ -535,7 +760,8 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) __maxnreg__((kernel_max_regs
   // after the merge.
   constexpr int MERGE_BYTES_STATE = NW * GMAX * (D + 4) * 4 + NW * GMAX * 2 * 4 + GMAX * 8;
   constexpr int MERGE_BYTES_FUSE = (3 * GMAX * kFuseCap + 4) * 4;  // fused combine scratch
-  static_assert(MERGE_BYTES_STATE <= STAGE_BYTES && MERGE_BYTES_FUSE <= STAGE_BYTES,
+  static_assert(Math::kRowOwning ||
+                    (MERGE_BYTES_STATE <= STAGE_BYTES && MERGE_BYTES_FUSE <= STAGE_BYTES),
                 "the merge fits in one stage");
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -750,7 +976,8 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) __maxnreg__((kernel_max_regs
         tok_end = min(tok_end, lim_base + ntok);
         // Phase 2 needs each row's count of visible keys: the partition-0
         // items (one per KV head, all equal) record it
-        if (part == 0 && lane < ntok && p.row_limit) p.row_limit[row0 + lane] = lim_base + lane + 1;
+        if (part == 0 && p.row_limit)
+          for (int t = lane; t < ntok; t += 32) p.row_limit[row0 + t] = lim_base + t + 1;
         if (tok_end <= tok_begin) {  // the partition lies past every token of the group
           item = grab_value(next_raw);
           continue;
@@ -836,10 +1063,11 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) __maxnreg__((kernel_max_regs
           }
         }
         if constexpr (Math::kChunk) {
-          if (first && lane < ntok) {  // one copy per token: its G heads are contiguous
+          // one copy per token: its G heads are contiguous
+          for (int t = lane; first && t < ntok; t += 32) {
             const T *q = static_cast<const T *>(p.query) +
-                         ((size_t)(row0 + lane) * p.num_heads + (size_t)kvh * p.group) * D;
-            bulk_load(ring_u32 + (uint32_t)st * STAGE_BYTES + 2 * HALF_BYTES + (uint32_t)(lane * qbytes), q,
+                         ((size_t)(row0 + t) * p.num_heads + (size_t)kvh * p.group) * D;
+            bulk_load(ring_u32 + (uint32_t)st * STAGE_BYTES + 2 * HALF_BYTES + (uint32_t)(t * qbytes), q,
                       (uint32_t)qbytes, full0 + 8 * st);
           }
         } else if (first && lane == 0) {
@@ -889,6 +1117,39 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) __maxnreg__((kernel_max_regs
         mbar_wait(full0 + 8 * (j % NST), (j / NST) & 1, kDrainLimitNs, nullptr);
     }
     __syncwarp();
+  } else if constexpr (Math::kRowOwning) {
+    // ============ consumer warps, each owning 16 rows of an item ============
+    Math math;
+    bool ok = true;
+    if (p.debug_flags & kDebugStallConsumers) {
+      // Wait on a barrier that nothing releases: the bound must end it.
+      ok = mbar_wait(never, 0, limit, flags);
+      ok = __all_sync(0xffffffffu, ok);
+    }
+    for (int i = 0; ok; ++i) {
+      const int st = i % NST;
+      const bool w = mbar_wait(full0 + 8 * st, (i / NST) & 1, limit, flags);
+      ok = __all_sync(0xffffffffu, w);
+      if (!ok) break;
+      const StageInfo h = info[st];
+      if (h.flags & kStageEnd) break;
+      const uint32_t kbase = ring_u32 + (uint32_t)st * STAGE_BYTES;
+      // h.np = the item's rows, h.pad = the key limit base of its first token
+      if (h.flags & kStageFirst)
+        math.begin_item(ring + (size_t)st * STAGE_BYTES + 2 * HALF_BYTES, h.np, lane, warp, h.pad,
+                        p.group);
+      math.tile(kbase, kbase + HALF_BYTES, geom, 0, min(ST, h.tok_end - h.tok0), lane,
+                p.scale_log2, h.tok0);
+      // nothing of the stage is read after the tile: hand it back at once
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty0 + 8 * st);
+      if (h.flags & kStageLast) math.finish(p, h.s, h.kvh, h.part, h.np, lane, warp);
+    }
+    if (!ok && lane == 0) {
+      report(p.status, kStatusTimeout);
+      flags[0] = 1;
+    }
+    pdl_launch_dependents();
   } else {
     // ======================= consumer warps =======================
     Math math;
@@ -1097,7 +1358,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) __maxnreg__((kernel_max_regs
 template <typename T, int D, int NW, int GMAX, class Math, bool SIMT>
 AttnKernelInfo attn_info() {
   return AttnKernelInfo{reinterpret_cast<const void *>(&pa_attn_kernel<T, D, NW, GMAX, Math, SIMT>),
-                        NW, NW * kTileTokens, GMAX};
+                        NW, stage_tokens<Math, NW>(), GMAX};
 }
 
 // Consumer warps per CTA: a stage is NW x 16 tokens; keep it at 32 KB of K+V
@@ -1126,9 +1387,21 @@ AttnKernelInfo select_tensor(int D, int group) {
   return AttnKernelInfo{nullptr, 0, 0, 0};
 }
 
-// Query chunks: the two-n-tile tensor path, 16 (token, head) rows an item.
+// Query chunks.  Chunks of more than 32 (token, head) rows per KV head run on
+// row-owning warps (64 keys a stage, items of 64 rows, four consumer warps)
+// for D 64 and 128 when the group divides 64; measured on GB300, that is
+// 1.3x the two-n-tile path at 16 and 64 tokens of 8 heads, while 32-row items
+// (two consumer warps, one per SM sub-partition) were slower than it at
+// 4 tokens.  Everything else runs on the two-n-tile tensor path, 16 rows an
+// item.
 template <typename T>
-AttnKernelInfo select_chunk(int D) {
+AttnKernelInfo select_chunk(int D, int group, int max_rows) {
+  if ((D == 64 || D == 128) && 64 % group == 0 && max_rows > 32) {
+    switch (D) {
+      case 64: return attn_info<T, 64, 4, 64, RowMath<T, 64, 4>, false>();
+      case 128: return attn_info<T, 128, 4, 64, RowMath<T, 128, 4>, false>();
+    }
+  }
   switch (D) {
     case 64: return attn_info<T, 64, consumer_warps<T, 64>(), 16, TensorMath<T, 64, 2, true>, false>();
     case 128: return attn_info<T, 128, consumer_warps<T, 128>(), 16, TensorMath<T, 128, 2, true>, false>();

@@ -3,6 +3,8 @@
 
 namespace pa {
 
-AttnKernelInfo attn_kernel_chunk_bf16(int head_size) { return select_chunk<__nv_bfloat16>(head_size); }
+AttnKernelInfo attn_kernel_chunk_bf16(int head_size, int group, int max_rows) {
+  return select_chunk<__nv_bfloat16>(head_size, group, max_rows);
+}
 
 }  // namespace pa

@@ -3,6 +3,8 @@
 
 namespace pa {
 
-AttnKernelInfo attn_kernel_chunk_f16(int head_size) { return select_chunk<__half>(head_size); }
+AttnKernelInfo attn_kernel_chunk_f16(int head_size, int group, int max_rows) {
+  return select_chunk<__half>(head_size, group, max_rows);
+}
 
 }  // namespace pa

@@ -86,8 +86,9 @@ enum MathKind { kMathSimt = 1, kMathTensor = 2 };
 struct AttnKernelInfo {
   const void *fn;     // __global__ function
   int consumer_warps; // warps computing; one more warp produces (TMA)
-  int stage_tokens;   // consumer_warps * kTileTokens
-  int max_group;      // largest H / Hkv it handles
+  int stage_tokens;   // tokens of one ring stage
+                      // (consumer_warps * kTileTokens, or 64 for row-owning warps)
+  int max_group;      // largest H / Hkv it handles (query chunks: rows of an item)
 };
 
 // Dynamic shared memory the attention kernel needs for `stages` stages (the
@@ -95,9 +96,9 @@ struct AttnKernelInfo {
 // a query slot padded to 1024 bytes; stage headers; mbarriers; flags;
 // CUDA-core tables).  The consumer warps merge inside an item's last stage, so
 // the merge takes no bytes of its own.
-inline size_t attn_smem_bytes(int head_size, int elt, int consumer_warps, int max_group,
-                              int stages, bool simt) {
-  const size_t kv = (size_t)consumer_warps * kTileTokens * head_size * elt * 2;
+inline size_t attn_smem_bytes(int head_size, int elt, int stage_tokens, int consumer_warps,
+                              int max_group, int stages, bool simt) {
+  const size_t kv = (size_t)stage_tokens * head_size * elt * 2;
   const size_t qslot = ((size_t)max_group * head_size * elt + 1023) & ~(size_t)1023;
   size_t ring = (kv + qslot) * stages;
   size_t headers = 32 * (size_t)stages;
@@ -117,8 +118,8 @@ AttnKernelInfo attn_kernel_tensor_f16(int head_size, int group);
 AttnKernelInfo attn_kernel_simt_f32(int head_size, int group);
 AttnKernelInfo attn_kernel_simt_bf16(int head_size, int group);
 AttnKernelInfo attn_kernel_simt_f16(int head_size, int group);
-AttnKernelInfo attn_kernel_chunk_bf16(int head_size);
-AttnKernelInfo attn_kernel_chunk_f16(int head_size);
+AttnKernelInfo attn_kernel_chunk_bf16(int head_size, int group, int max_rows);
+AttnKernelInfo attn_kernel_chunk_f16(int head_size, int group, int max_rows);
 const void *reduce_kernel(int dtype, int float4_per_thread);
 const void *stage_in_kernel();
 

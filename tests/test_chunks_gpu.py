@@ -122,3 +122,25 @@ def test_bench_chunk_workload_full_size():
                          c.partition_size, ws, max_seq_len=c.max_seq_len, max_chunk=4)
     assert pa.pa_read_device_status(ws) == pa.PA_OK
     assert_close(out, ref, c.dtype, "c4 cache, 4-token chunks")
+
+
+def test_long_chunk_workload_full_size():
+    """Long chunks at full size: the c4_batch256 cache with a 64-token causal
+    chunk per sequence (16384 query rows, 512 (token, head) rows per KV head,
+    run as 64-row items on row-owning warps), V2 and V1, every output
+    against the oracle; the benchmark's `long_chunks` entry runs this step."""
+    c = workloads.config_case("c4_batch256")
+    q, qs = workloads.chunk_queries(c, 64)
+    ref = oracle.query_chunks(q, c.key_cache, c.value_cache, c.block_tables, c.seq_lens, qs,
+                              c.scale)
+    dev = "cuda"
+    R, H, D = q.shape
+    ws = pa.alloc_workspace(R, H, D, c.max_seq_len, c.partition_size)
+    args = (q.to(dev), c.key_cache.to(dev), c.value_cache.to(dev), c.block_tables.to(dev),
+            c.seq_lens.to(dev), qs.to(dev))
+    for variant in (pa.PA_VARIANT_V2, pa.PA_VARIANT_V1):
+        out = torch.full((R, H, D), float("nan"), dtype=c.dtype, device=dev)
+        pa.pa_chunks_forward(out, *args, c.scale, c.partition_size, ws,
+                             max_seq_len=c.max_seq_len, max_chunk=64, variant=variant)
+        assert pa.pa_read_device_status(ws) == pa.PA_OK
+        assert_close(out, ref, c.dtype, f"c4 cache, 64-token chunks, v{variant}")
