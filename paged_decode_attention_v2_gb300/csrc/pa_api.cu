@@ -145,9 +145,10 @@ pa_status_t get_encoder(PFN_cuTensorMapEncodeTiled_v12000 *fn) {
   return PA_OK;
 }
 
-// A 2-D view of a cache: rows = num_blocks * num_kv_heads * block_size token
-// rows of head_size elements; the box is one 128-byte panel x unit_rows rows,
-// landing in shared memory with the 128-byte swizzle.
+// A 3-D view of a cache: (128-byte panel slice, token row, panel), the rows
+// being the num_blocks * num_kv_heads * block_size token rows of head_size
+// elements; the box is a whole unit of unit_rows rows (every panel), landing
+// in shared memory as [panel][row][128 bytes] with the 128-byte swizzle.
 pa_status_t encode_cache_map(CUtensorMap *map, const void *base, int dtype, int head_size,
                              long long rows, int unit_rows) {
   PFN_cuTensorMapEncodeTiled_v12000 enc;
@@ -157,11 +158,13 @@ pa_status_t encode_cache_map(CUtensorMap *map, const void *base, int dtype, int 
   CUtensorMapDataType dt = dtype == PA_DTYPE_F32    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
                            : dtype == PA_DTYPE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                                     : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-  cuuint64_t gdim[2] = {(cuuint64_t)head_size, (cuuint64_t)rows};
-  cuuint64_t gstride[1] = {(cuuint64_t)head_size * elt};
-  cuuint32_t box[2] = {(cuuint32_t)(kPanelBytes / elt), (cuuint32_t)unit_rows};
-  cuuint32_t estride[2] = {1, 1};
-  CUresult r = enc(map, dt, 2, const_cast<void *>(base), gdim, gstride, box, estride,
+  const int panel = kPanelBytes / elt;  // elements of a 128-byte panel
+  const int panels = head_size / panel;
+  cuuint64_t gdim[3] = {(cuuint64_t)panel, (cuuint64_t)rows, (cuuint64_t)panels};
+  cuuint64_t gstride[2] = {(cuuint64_t)head_size * elt, (cuuint64_t)kPanelBytes};
+  cuuint32_t box[3] = {(cuuint32_t)panel, (cuuint32_t)unit_rows, (cuuint32_t)panels};
+  cuuint32_t estride[3] = {1, 1, 1};
+  CUresult r = enc(map, dt, 3, const_cast<void *>(base), gdim, gstride, box, estride,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {

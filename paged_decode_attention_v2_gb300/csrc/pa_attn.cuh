@@ -961,7 +961,11 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) __maxnreg__((attn_max_regs<M
         }
       }
       if (!found) break;
-      const int next_raw = grab_issue();  // its latency overlaps this item's stages
+      // The next item is taken from the counter once this item's first copies
+      // are issued: nothing needs it before the item ends, and every CTA
+      // reaches this point at about the same moment, so the atomics queue on
+      // one address for a while.
+      int next_raw = 0;
 
       const int tok_begin = part * p.range_tokens;
       int tok_end = min(tok_begin + p.range_tokens, L);
@@ -979,14 +983,14 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) __maxnreg__((attn_max_regs<M
         if (part == 0 && p.row_limit)
           for (int t = lane; t < ntok; t += 32) p.row_limit[row0 + t] = lim_base + t + 1;
         if (tok_end <= tok_begin) {  // the partition lies past every token of the group
-          item = grab_value(next_raw);
+          item = grab_value(grab_issue());
           continue;
         }
       }
       if (tok_end <= tok_begin) {  // empty sequence (V1, or V2 with the fused combine): zeros
         T *o = static_cast<T *>(p.out) + ((size_t)s * p.num_heads + (size_t)kvh * p.group) * D;
         for (int e = lane; e < p.group * D; e += 32) o[e] = from_float<T>(0.f);
-        item = grab_value(next_raw);
+        item = grab_value(grab_issue());
         continue;
       }
       // A window of 64 block-table entries: lane j holds pages win0+j (cur)
@@ -1047,19 +1051,13 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) __maxnreg__((attn_max_regs<M
         if (y >= 0) {
           const uint32_t kdst = ring_u32 + (uint32_t)st * STAGE_BYTES + (uint32_t)lane * geom.unit_bytes;
           const uint32_t vdst = kdst + HALF_BYTES;
-#pragma unroll
-          for (int pn = 0; pn < NPANELS; ++pn) {
-            if constexpr (Math::kChunk) {  // the next row group re-reads these pages: keep them
-              tma_load_2d(kdst + pn * geom.panel_bytes, &tmap_k, pn * (kPanelBytes / ELT), y,
-                          full0 + 8 * st);
-              tma_load_2d(vdst + pn * geom.panel_bytes, &tmap_v, pn * (kPanelBytes / ELT), y,
-                          full0 + 8 * st);
-            } else {
-              tma_load_2d_hint(kdst + pn * geom.panel_bytes, &tmap_k, pn * (kPanelBytes / ELT), y,
-                               full0 + 8 * st, kv_policy);
-              tma_load_2d_hint(vdst + pn * geom.panel_bytes, &tmap_v, pn * (kPanelBytes / ELT), y,
-                               full0 + 8 * st, kv_policy);
-            }
+          // one copy per page and tensor: all panels of the unit's rows
+          if constexpr (Math::kChunk) {  // the next row group re-reads these pages: keep them
+            tma_load_3d(kdst, &tmap_k, 0, y, 0, full0 + 8 * st);
+            tma_load_3d(vdst, &tmap_v, 0, y, 0, full0 + 8 * st);
+          } else {
+            tma_load_3d_hint(kdst, &tmap_k, 0, y, 0, full0 + 8 * st, kv_policy);
+            tma_load_3d_hint(vdst, &tmap_v, 0, y, 0, full0 + 8 * st, kv_policy);
           }
         }
         if constexpr (Math::kChunk) {
@@ -1076,6 +1074,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) __maxnreg__((attn_max_regs<M
           bulk_load(ring_u32 + (uint32_t)st * STAGE_BYTES + 2 * HALF_BYTES, q, (uint32_t)qbytes,
                     full0 + 8 * st);
         }
+        if (j == 0) next_raw = grab_issue();
         ++i;
         const int next_rel = ((stage_tok0 + ST) >> p.log2_block_size) - win0;
         if (next_rel >= 32) {
