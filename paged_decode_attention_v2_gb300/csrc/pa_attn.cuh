@@ -328,10 +328,14 @@ struct RowMath {
   static constexpr bool kChunk = true;
   static constexpr bool kRowOwning = true;
   static constexpr int ST = 64;          // keys per stage
+  // keys of one softmax step: at D = 128 a stage is taken in two halves, so
+  // that S and P of only 32 keys are live beside O and the queries and a
+  // thread fits in 168 registers (two CTAs an SM)
+  static constexpr int SK = D >= 128 ? 32 : 64;
   static constexpr int KS = D / 16;      // k-steps of S = Q K^T
-  static constexpr int NK = ST / 8;      // key n-tiles of S
+  static constexpr int NK = SK / 8;      // key n-tiles of S
   static constexpr int ND = D / 8;       // d n-tiles of O
-  static constexpr int KK = ST / 16;     // key k-steps of O += P V
+  static constexpr int KK = SK / 16;     // key k-steps of O += P V
   static constexpr int GMAX = 16 * NWC;  // rows of an item
   uint32_t qa[KS][4];  // A fragments of this warp's 16 query rows
   float o[ND][4];
@@ -364,8 +368,17 @@ struct RowMath {
   }
 
   // One stage: keys [abs0, abs0 + valid) of the item, at positions 0.. of
-  // the stage buffers.
+  // the stage buffers, SK keys at a time.
   __device__ __forceinline__ void tile(uint32_t kbase, uint32_t vbase, const StageGeom &g, int,
+                                       int valid, int lane, float scale_log2, int abs0) {
+#pragma unroll
+    for (int k0 = 0; k0 < ST; k0 += SK)
+      if (k0 < valid) step(kbase, vbase, g, k0, valid - k0, lane, scale_log2, abs0 + k0);
+  }
+
+  // Keys [abs0, abs0 + valid) at positions key0.. of the stage buffers (only
+  // the first SK of them).
+  __device__ __forceinline__ void step(uint32_t kbase, uint32_t vbase, const StageGeom &g, int key0,
                                        int valid, int lane, float scale_log2, int abs0) {
     const int mi = lane >> 3, r = lane & 7, q4 = lane & 3;
     // ---- S = Q K^T: matrix mi of an ldmatrix.x4 is keys 16 jp + r + 8 (mi >> 1)
@@ -381,7 +394,7 @@ struct RowMath {
       int ktok[NK / 2];
 #pragma unroll
       for (int jp = 0; jp < NK / 2; ++jp) {
-        ktok[jp] = 16 * jp + r + ((mi >> 1) << 3);
+        ktok[jp] = key0 + 16 * jp + r + ((mi >> 1) << 3);
         krow[jp] = g.row_addr(kbase, ktok[jp]);
       }
 #pragma unroll
@@ -400,7 +413,7 @@ struct RowMath {
     for (int j = 0; j < NK; ++j)
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const int kr = 8 * j + 2 * q4 + (e & 1);  // key within the stage
+        const int kr = 8 * j + 2 * q4 + (e & 1);  // key within the step
         float x = s[j][e] * scale_log2;
         if (kr >= valid || abs0 + kr >= lim[e >> 1]) x = -CUDART_INF_F;
         s[j][e] = x;
@@ -456,10 +469,10 @@ struct RowMath {
     const int k0 = 2 * q4;
 #pragma unroll
     for (int kk = 0; kk < KK; ++kk) {
-      const int tk = 16 * kk + r + ((mi & 1) << 3);
+      const int tk = key0 + 16 * kk + r + ((mi & 1) << 3);
       const uint32_t vrow = g.row_addr(vbase, tk);
       uint32_t keep_lo = 0xffffffffu, keep_hi = 0xffffffffu;  // keys 16 kk + k0 (+1), and + 8
-      if (valid < ST) {
+      if (valid < SK) {
         const int a = 16 * kk + k0;
         keep_lo = (a < valid ? 0x0000ffffu : 0u) | (a + 1 < valid ? 0xffff0000u : 0u);
         keep_hi = (a + 8 < valid ? 0x0000ffffu : 0u) | (a + 9 < valid ? 0xffff0000u : 0u);
@@ -721,11 +734,12 @@ constexpr int kernel_max_regs() {
   return GMAX > 8 ? (NW == 4 ? 168 : 255) : (NW == 4 ? 128 : (NW == 2 ? 168 : 255));
 }
 
-// Row-owning query chunks: two CTAs per SM (their shared memory allows no
-// more), so with 4 consumer warps (5 warps a CTA) up to 204 registers fit.
+// Row-owning query chunks: two CTAs of 5 warps put 3 warps on some
+// schedulers, so 168 registers a thread at most (at 200 an SM held one CTA,
+// one consumer warp per scheduler).
 template <class Math, int NW, int GMAX>
 constexpr int attn_max_regs() {
-  return Math::kRowOwning ? (NW == 4 ? 200 : 255) : kernel_max_regs<NW, GMAX>();
+  return Math::kRowOwning ? (NW == 4 ? 168 : 255) : kernel_max_regs<NW, GMAX>();
 }
 
 // Tokens of one ring stage: 16 per consumer warp, or 64 for row-owning warps
