@@ -363,8 +363,9 @@ class ChunkRunner:
         self.q = q
         self.tokens = tokens
         sm = torch.cuda.get_device_properties(device).multi_processor_count
-        self.is_v2 = bool(pa.pa_choose_v2(case.num_seqs, case.num_kv_heads, case.max_seq_len,
-                                          case.partition_size, sm))
+        self.is_v2 = bool(pa.pa_choose_v2_chunks(case.num_seqs, case.num_heads,
+                                                 case.num_kv_heads, case.head_size, tokens,
+                                                 case.max_seq_len, case.partition_size, sm))
         self.has_phase2 = self.is_v2
         self.kernels_per_step = 2 if self.is_v2 else 1
         self.ws = pa.alloc_workspace(q.shape[0], case.num_heads, case.head_size,

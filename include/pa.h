@@ -335,6 +335,18 @@ pa_status_t pa_v2_forward_noalloc(void *out, const void *query,
 int pa_choose_v2(int num_seqs, int num_kv_heads, int max_seq_len,
                  int partition_size, int sm_count);
 
+/* The same heuristic for query chunks (pa_chunks_forward with the automatic
+ * variant): 1 for V2, 0 for V1, for chunks of at most max_chunk tokens.  V1
+ * when every sequence fits in one partition; with at most 8 (token, head)
+ * rows per KV head, pa_choose_v2's answer; otherwise V1 when the batch has
+ * at least 8 work items per SM, counting an item per (sequence, KV head) and
+ * row group as the chunk kernels cut them (64 rows on the row-owning kernel:
+ * more than 32 rows per KV head, head_size 64 or 128, a group dividing 64;
+ * else 16), V2 below (measured on GB300).  Pure host arithmetic on its
+ * arguments. */
+int pa_choose_v2_chunks(int num_seqs, int num_heads, int num_kv_heads, int head_size,
+                        int max_chunk, int max_seq_len, int partition_size, int sm_count);
+
 /* Synchronise `stream`, return the workspace's status word as a pa_status_t
  * (PA_OK if no kernel reported a problem) and reset it to 0.  The pages have
  * no counterpart: this is how the library reports data errors its kernels

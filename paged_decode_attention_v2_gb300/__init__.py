@@ -40,7 +40,7 @@ _DTYPES = {torch.float32: PA_DTYPE_F32, torch.bfloat16: PA_DTYPE_BF16,
 
 # Every function the header declares (checked against include/pa.h by tests).
 EXPORTS = ("pa_workspace_bytes", "pa_workspace_layout", "pa_workspace_init",
-           "pa_v1_forward", "pa_v2_forward", "pa_forward", "pa_choose_v2",
+           "pa_v1_forward", "pa_v2_forward", "pa_forward", "pa_choose_v2", "pa_choose_v2_chunks",
            "pa_read_device_status", "pa_status_string", "pa_last_cuda_error",
            "pa_version", "pa_v2_forward_noalloc", "pa_host_staging_bytes", "pa_forward_host",
            "pa_chunks_forward", "pa_v2_partials", "pa_v2_combine")
@@ -108,6 +108,8 @@ def load_library(path: str = LIB_PATH):
                                         [ctypes.POINTER(pa_options_t)])
         lib.pa_choose_v2.restype = ci
         lib.pa_choose_v2.argtypes = [ci] * 5
+        lib.pa_choose_v2_chunks.restype = ci
+        lib.pa_choose_v2_chunks.argtypes = [ci] * 8
         lib.pa_read_device_status.restype = ci
         lib.pa_read_device_status.argtypes = [vp, vp]
         lib.pa_status_string.restype = ctypes.c_char_p
@@ -340,6 +342,14 @@ def pa_choose_v2(num_seqs: int, num_kv_heads: int, max_seq_len: int, partition_s
                  sm_count: int) -> int:
     return int(load_library().pa_choose_v2(num_seqs, num_kv_heads, max_seq_len,
                                            partition_size, sm_count))
+
+
+def pa_choose_v2_chunks(num_seqs: int, num_heads: int, num_kv_heads: int, head_size: int,
+                        max_chunk: int, max_seq_len: int, partition_size: int,
+                        sm_count: int) -> int:
+    return int(load_library().pa_choose_v2_chunks(num_seqs, num_heads, num_kv_heads, head_size,
+                                                  max_chunk, max_seq_len, partition_size,
+                                                  sm_count))
 
 
 def pa_read_device_status(workspace: torch.Tensor, stream=None) -> int:

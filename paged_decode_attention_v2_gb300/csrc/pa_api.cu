@@ -641,8 +641,11 @@ pa_status_t resolve(const Call &c, int variant, bool *v2) {
     DeviceFacts *dev = nullptr;
     pa_status_t st = device_facts(&dev);
     if (st != PA_OK) return st;
-    *v2 = pa_choose_v2(c.num_seqs, c.num_kv_heads, c.max_seq_len, c.partition_size,
-                       dev->sm_count) != 0;
+    *v2 = (c.q_start ? pa_choose_v2_chunks(c.num_seqs, c.num_heads, c.num_kv_heads, c.head_size,
+                                           c.max_chunk, c.max_seq_len, c.partition_size,
+                                           dev->sm_count)
+                     : pa_choose_v2(c.num_seqs, c.num_kv_heads, c.max_seq_len,
+                                    c.partition_size, dev->sm_count)) != 0;
   } else {
     return PA_ERR_INVALID_ARG;
   }
@@ -954,6 +957,32 @@ int pa_choose_v2(int num_seqs, int num_kv_heads, int max_seq_len, int partition_
   if (items >= 16 * sm) return 0;
   if (items >= 8 * sm && max_seq_len <= 2LL * partition_size) return 0;
   if (items >= 2 * sm && items <= 3 * sm && max_seq_len <= 4LL * partition_size) return 0;
+  return 1;
+}
+
+int pa_choose_v2_chunks(int num_seqs, int num_heads, int num_kv_heads, int head_size,
+                        int max_chunk, int max_seq_len, int partition_size, int sm_count) {
+  if (partition_size < 1 || max_seq_len <= partition_size) return 0;
+  if (sm_count <= 0 || num_kv_heads < 1 || num_heads < num_kv_heads || max_chunk < 1) return 1;
+  const int group = num_heads / num_kv_heads;
+  const long long rows = (long long)max_chunk * group;
+  // Up to 8 (token, head) rows per KV head the item costs what a decode item
+  // does: the decode rule holds.
+  if (rows <= 8)
+    return pa_choose_v2(num_seqs, num_kv_heads, max_seq_len, partition_size, sm_count);
+  // Items as the chunk kernels cut them: 64 rows on row-owning warps, else 16.
+  const bool row_owning = (head_size == 64 || head_size == 128) && 64 % group == 0 && rows > 32;
+  const int tokens = (row_owning ? 64 : 16) / group;
+  const long long groups = (max_chunk + tokens - 1) / tokens;
+  const long long items = (long long)num_seqs * num_kv_heads * groups;
+  // Measured on GB300 (bf16, D 128, 32 q / 4 kv heads; 256 sequences of up
+  // to 3584 tokens with 2 to 64 tokens a chunk, 8 of up to 8192 and one of
+  // 100,000; consecutive steps): V1 is ahead from 2048 items (13.5 per SM:
+  // 1.23x at 4 tokens, 1.03x at 16, 1.18x at 64), V2 at 1024 items and fewer
+  // (6.7 per SM: 1.02x at 2 tokens, 1.12x at 8).  A chunk item's epilogue
+  // costs more than a decode item's, and V1 pays it once per sequence; the
+  // switch sits between the two measured counts.
+  if (items >= 8LL * sm_count) return 0;
   return 1;
 }
 

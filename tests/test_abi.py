@@ -91,6 +91,34 @@ def test_choose_v2_matches_the_measured_crossover(lib, cell):
     assert pa.pa_choose_v2(bh // 4, 4, L, 512, 152) == CHOOSE_V2_MEASURED[cell]
 
 
+# Query chunks, measured on GB300 (bf16, D 128, consecutive steps): (workload,
+# tokens a chunk): faster variant.  c4: 256 sequences of up to 3584 tokens, 32 q /
+# 4 kv heads; c2: 8 sequences of up to 8192; c3: one of 100,000.
+CHUNK_SHAPES = {"c4": (256, 32, 4, 128, 3584), "c2": (8, 32, 4, 128, 8192),
+                "c3": (1, 32, 4, 128, 100000)}
+CHOOSE_V2_CHUNKS_MEASURED = {
+    ("c4", 2): 1, ("c4", 4): 0, ("c4", 8): 1, ("c4", 16): 0, ("c4", 64): 0,
+    ("c2", 4): 1, ("c2", 16): 1, ("c2", 64): 1, ("c3", 16): 1, ("c3", 64): 1,
+}
+
+
+@pytest.mark.parametrize("cell", sorted(CHOOSE_V2_CHUNKS_MEASURED))
+def test_choose_v2_chunks_matches_the_measured_cells(lib, cell):
+    B, H, Hkv, D, L = CHUNK_SHAPES[cell[0]]
+    got = pa.pa_choose_v2_chunks(B, H, Hkv, D, cell[1], L, 512, 152)
+    assert got == CHOOSE_V2_CHUNKS_MEASURED[cell]
+
+
+def test_choose_v2_chunks_small_rows_follow_decode(lib):
+    # up to 8 rows per KV head (1 token of 8 heads, 2 of 4): the decode rule
+    for B, L in ((256, 3584), (8, 8192), (4096, 1024), (1, 100000)):
+        assert pa.pa_choose_v2_chunks(B, 32, 4, 128, 1, L, 512, 152) == \
+            pa.pa_choose_v2(B, 4, L, 512, 152)
+        assert pa.pa_choose_v2_chunks(B, 16, 4, 128, 2, L, 512, 152) == \
+            pa.pa_choose_v2(B, 4, L, 512, 152)
+    assert pa.pa_choose_v2_chunks(256, 32, 4, 128, 16, 500, 512, 152) == 0  # one partition
+
+
 @pytest.mark.parametrize("args,expect", [
     ((1, 4, 100000, 512, 152), 1),   # one long sequence: V2 spreads it over the GPU
     ((8, 4, 8192, 512, 152), 1),     # few (seq, kv head) items: V2
