@@ -96,6 +96,11 @@ typedef struct {
  * path without hanging or faulting the GPU. */
 #define PA_DEBUG_STALL_CONSUMERS 1
 
+/* Debug: query chunks never take the tcgen05 kernel (chunks of at least 128
+ * rows per KV head at head_size 128 then run on the mma.sync row-owning
+ * kernel), for comparisons of the two. */
+#define PA_DEBUG_NO_TCGEN05 2
+
 /* Bytes of workspace that pa_v2_forward needs (V1 needs only the 256-byte
  * status block).  The partials are the three per-partition arrays that the
  * "paged_attention_v2" commit note (project_6, commit 96f4baf "Dockerfile",
@@ -339,11 +344,12 @@ int pa_choose_v2(int num_seqs, int num_kv_heads, int max_seq_len,
  * variant): 1 for V2, 0 for V1, for chunks of at most max_chunk tokens.  V1
  * when every sequence fits in one partition; with at most 8 (token, head)
  * rows per KV head, pa_choose_v2's answer; otherwise V1 when the batch has
- * at least 8 work items per SM, counting an item per (sequence, KV head) and
- * row group as the chunk kernels cut them (64 rows on the row-owning kernel:
- * more than 32 rows per KV head, head_size 64 or 128, a group dividing 64;
- * else 16), V2 below (measured on GB300).  Pure host arithmetic on its
- * arguments. */
+ * at least 8 work items per SM (4 on the tcgen05 kernel), counting an item
+ * per (sequence, KV head) and row group as the chunk kernels cut them (128
+ * rows on the tcgen05 kernel: at least 128 rows per KV head at head_size
+ * 128; 64 on the row-owning kernel: more than 32 rows per KV head,
+ * head_size 64 or 128, a group dividing 64; else 16), V2 below (measured on
+ * GB300).  Pure host arithmetic on its arguments. */
 int pa_choose_v2_chunks(int num_seqs, int num_heads, int num_kv_heads, int head_size,
                         int max_chunk, int max_seq_len, int partition_size, int sm_count);
 

@@ -34,6 +34,7 @@ PA_DTYPE_F32, PA_DTYPE_BF16, PA_DTYPE_F16 = 0, 1, 2
 PA_VARIANT_AUTO, PA_VARIANT_V1, PA_VARIANT_V2 = 0, 1, 2
 PA_MATH_AUTO, PA_MATH_SIMT, PA_MATH_TENSOR = 0, 1, 2
 PA_DEBUG_STALL_CONSUMERS = 1
+PA_DEBUG_NO_TCGEN05 = 2
 
 _DTYPES = {torch.float32: PA_DTYPE_F32, torch.bfloat16: PA_DTYPE_BF16,
            torch.float16: PA_DTYPE_F16}
@@ -278,7 +279,7 @@ def pa_forward(out, query, key_cache, value_cache, block_tables, seq_lens, scale
 def pa_chunks_forward(out, query, key_cache, value_cache, block_tables, seq_lens, q_start,
                       scale, partition_size, workspace, max_seq_len=None, max_chunk=None,
                       stream=None, variant=PA_VARIANT_AUTO, num_stages=0, ctas_per_sm=0,
-                      phase1_event=None) -> None:
+                      phase1_event=None, debug_flags=0) -> None:
     """Multi-token queries over the paged cache (see include/pa.h): query and
     out [num_rows, H, D]; the chunk of sequence s is rows q_start[s] ..
     q_start[s+1]-1 (int32 on the device), its last tokens.  max_chunk bounds
@@ -293,8 +294,8 @@ def pa_chunks_forward(out, query, key_cache, value_cache, block_tables, seq_lens
     if max_seq_len is None:
         max_seq_len = block_tables.shape[1] * bs
     mc = int(max_chunk) if max_chunk is not None else int(max_seq_len)
-    opts = pa_options_t(variant, PA_MATH_AUTO, num_stages, 0, 0, _event_handle(phase1_event),
-                        ctas_per_sm, 0)
+    opts = pa_options_t(variant, PA_MATH_AUTO, num_stages, debug_flags, 0,
+                        _event_handle(phase1_event), ctas_per_sm, 0)
     _check(load_library().pa_chunks_forward(
         _ptr(out), _ptr(query), _ptr(key_cache), _ptr(value_cache), _ptr(block_tables),
         _ptr(seq_lens), _ptr(q_start), B, R, mc, H, hkv, D, nb, bs, block_tables.shape[1],

@@ -41,6 +41,7 @@ struct DeviceFacts {
   bool ready = false;
   int sm_count = 0;
   int max_smem_optin = 0;
+  int smem_per_sm = 0, reserved_smem = 0, regs_per_sm = 0, threads_per_sm = 0;
 };
 constexpr int kMaxDevices = 64;
 DeviceFacts g_devices[kMaxDevices];
@@ -58,9 +59,35 @@ pa_status_t device_facts(DeviceFacts **out) {
     if (e != cudaSuccess) return fail_cuda("cudaDeviceGetAttribute(SM count)", e);
     e = cudaDeviceGetAttribute(&f.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     if (e != cudaSuccess) return fail_cuda("cudaDeviceGetAttribute(smem)", e);
+    e = cudaDeviceGetAttribute(&f.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+    if (e != cudaSuccess) return fail_cuda("cudaDeviceGetAttribute(smem per SM)", e);
+    e = cudaDeviceGetAttribute(&f.reserved_smem, cudaDevAttrReservedSharedMemoryPerBlock, dev);
+    if (e != cudaSuccess) return fail_cuda("cudaDeviceGetAttribute(reserved smem)", e);
+    e = cudaDeviceGetAttribute(&f.regs_per_sm, cudaDevAttrMaxRegistersPerMultiprocessor, dev);
+    if (e != cudaSuccess) return fail_cuda("cudaDeviceGetAttribute(registers)", e);
+    e = cudaDeviceGetAttribute(&f.threads_per_sm, cudaDevAttrMaxThreadsPerMultiProcessor, dev);
+    if (e != cudaSuccess) return fail_cuda("cudaDeviceGetAttribute(threads)", e);
     f.ready = true;
   }
   *out = &f;
+  return PA_OK;
+}
+
+// CTAs of a kernel one SM holds by its registers (whole warps, 256-register
+// allocation units), shared memory (with the per-block reservation) and
+// threads.
+pa_status_t resource_ctas_per_sm(const void *fn, int threads, size_t smem, const DeviceFacts *dev,
+                                 int *out) {
+  cudaFuncAttributes fa;
+  cudaError_t e = cudaFuncGetAttributes(&fa, fn);
+  if (e != cudaSuccess) return fail_cuda("cudaFuncGetAttributes", e);
+  const long long warps = (threads + 31) / 32;
+  const long long regs_per_warp = ((long long)fa.numRegs * 32 + 255) / 256 * 256;
+  long long n = regs_per_warp > 0 ? dev->regs_per_sm / (warps * regs_per_warp) : 0;
+  const long long per_block = (long long)smem + fa.sharedSizeBytes + dev->reserved_smem;
+  if (per_block > 0 && dev->smem_per_sm / per_block < n) n = dev->smem_per_sm / per_block;
+  if (dev->threads_per_sm / threads < n) n = dev->threads_per_sm / threads;
+  *out = (int)(n > 0 ? n : 0);
   return PA_OK;
 }
 
@@ -291,6 +318,32 @@ AttnKernelInfo pick_kernel(int math, int dtype, int head_size, int group) {
   return AttnKernelInfo{nullptr, 0, 0, 0};
 }
 
+// The cache as TMA sees it for the tcgen05 chunk kernel: rows of head_size
+// elements, a box of one 128-byte panel x unit_rows rows (a stage keeps each
+// panel's rows together: [panel][row][128 bytes]).
+pa_status_t encode_cache_map_2d(CUtensorMap *map, const void *base, int dtype, int head_size,
+                                long long rows, int unit_rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc;
+  pa_status_t st = get_encoder(&enc);
+  if (st != PA_OK) return st;
+  const int elt = elt_size(dtype);
+  CUtensorMapDataType dt = dtype == PA_DTYPE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                  : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  cuuint64_t gdim[2] = {(cuuint64_t)head_size, (cuuint64_t)rows};
+  cuuint64_t gstride[1] = {(cuuint64_t)head_size * elt};
+  cuuint32_t box[2] = {(cuuint32_t)(kPanelBytes / elt), (cuuint32_t)unit_rows};
+  cuuint32_t estride[2] = {1, 1};
+  CUresult r = enc(map, dt, 2, const_cast<void *>(base), gdim, gstride, box, estride,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    char msg[64];
+    snprintf(msg, sizeof msg, "CUresult %d", (int)r);
+    return fail_cuda("cuTensorMapEncodeTiled", msg);
+  }
+  return PA_OK;
+}
+
 // Phase 2 of one call: kernel, grid and parameters.  It is planned before
 // Phase 1 is enqueued, so that nothing can fail between the two launches.
 struct Phase2Plan {
@@ -406,11 +459,14 @@ pa_status_t launch(const Call &c, bool v2, const pa_options_t &opt) {
   if (math == kMathTensor && c.dtype == PA_DTYPE_F32) return PA_ERR_UNSUPPORTED;
   const bool chunk = c.q_start != nullptr;
   if (chunk && math != kMathTensor) return PA_ERR_UNSUPPORTED;
+  const bool umma = chunk && !(opt.debug_flags & PA_DEBUG_NO_TCGEN05) &&
+                    umma_chunk_ok(c.head_size, group, (long long)c.max_chunk * group);
   const AttnKernelInfo k =
-      chunk ? (c.dtype == PA_DTYPE_BF16
-                   ? attn_kernel_chunk_bf16(c.head_size, group, c.max_chunk * group)
-                   : attn_kernel_chunk_f16(c.head_size, group, c.max_chunk * group))
-            : pick_kernel(math, c.dtype, c.head_size, group);
+      umma    ? attn_kernel_umma_chunk(c.dtype == PA_DTYPE_BF16 ? 1 : 0)
+      : chunk ? (c.dtype == PA_DTYPE_BF16
+                     ? attn_kernel_chunk_bf16(c.head_size, group, c.max_chunk * group)
+                     : attn_kernel_chunk_f16(c.head_size, group, c.max_chunk * group))
+              : pick_kernel(math, c.dtype, c.head_size, group);
   if (!k.fn) return PA_ERR_UNSUPPORTED;
 
   const int elt = elt_size(c.dtype);
@@ -424,6 +480,7 @@ pa_status_t launch(const Call &c, bool v2, const pa_options_t &opt) {
   // than two CTAs of three).
   int stages = opt.num_stages > 0 ? opt.num_stages : 0;
   if (stages > 0 && (stages < 2 || stages > 16)) return PA_ERR_INVALID_ARG;
+  if (k.umma) stages = kUmmaStagesHost;  // a fixed layout
   if (stages == 0) {
     long long best = 0;
     for (int n = 2; n <= 8; ++n) {
@@ -443,16 +500,18 @@ pa_status_t launch(const Call &c, bool v2, const pa_options_t &opt) {
     }
     if (stages <= 0) return PA_ERR_UNSUPPORTED;
   }
-  size_t smem = attn_smem_bytes(c.head_size, elt, k.stage_tokens, k.consumer_warps, k.max_group,
-                                stages, simt);
+  size_t smem = k.umma ? umma_chunk_smem_bytes()
+                      : attn_smem_bytes(c.head_size, elt, k.stage_tokens, k.consumer_warps,
+                                        k.max_group, stages, simt);
   if (smem > (size_t)dev->max_smem_optin) return PA_ERR_UNSUPPORTED;
 
   const int unit_rows = c.block_size < k.stage_tokens ? c.block_size : k.stage_tokens;
   const long long rows = (long long)c.num_blocks * c.num_kv_heads * c.block_size;
   CUtensorMap tmap_k, tmap_v;
-  st = encode_cache_map(&tmap_k, c.key_cache, c.dtype, c.head_size, rows, unit_rows);
+  auto encode = k.umma ? encode_cache_map_2d : encode_cache_map;
+  st = encode(&tmap_k, c.key_cache, c.dtype, c.head_size, rows, unit_rows);
   if (st != PA_OK) return st;
-  st = encode_cache_map(&tmap_v, c.value_cache, c.dtype, c.head_size, rows, unit_rows);
+  st = encode(&tmap_v, c.value_cache, c.dtype, c.head_size, rows, unit_rows);
   if (st != PA_OK) return st;
 
   uint8_t *ws = static_cast<uint8_t *>(c.workspace);
@@ -546,6 +605,20 @@ pa_status_t launch(const Call &c, bool v2, const pa_options_t &opt) {
   if (st != PA_OK) return st;
   if (per_sm < 1) return PA_ERR_UNSUPPORTED;
   if (opt.ctas_per_sm > 0 && opt.ctas_per_sm < per_sm) per_sm = opt.ctas_per_sm;
+  if (k.umma) {
+    // The occupancy query answers 1 for this kernel whatever its shared
+    // memory (measured on GB300: at 20 KB too), while two CTAs fit its
+    // registers, shared memory and tensor memory and do run side by side
+    // (1.5x the throughput of one).  So its CTAs per SM come from those
+    // resources, never more than the 512 tensor-memory columns hold.  A CTA
+    // the SM cannot place would only start late: CTAs never wait on others.
+    int est = 0;
+    st = resource_ctas_per_sm(k.fn, threads, smem, dev, &est);
+    if (st != PA_OK) return st;
+    if (est > per_sm) per_sm = est;
+    if (opt.ctas_per_sm > 0 && opt.ctas_per_sm < per_sm) per_sm = opt.ctas_per_sm;
+    if (per_sm * kUmmaTmemColsHost > 512) per_sm = 512 / kUmmaTmemColsHost;
+  }
   const long long range_parts =
       v2 ? (long long)(c.part_end < p.max_parts ? c.part_end : p.max_parts) - c.part_begin
          : p.max_parts;
@@ -970,19 +1043,22 @@ int pa_choose_v2_chunks(int num_seqs, int num_heads, int num_kv_heads, int head_
   // does: the decode rule holds.
   if (rows <= 8)
     return pa_choose_v2(num_seqs, num_kv_heads, max_seq_len, partition_size, sm_count);
-  // Items as the chunk kernels cut them: 64 rows on row-owning warps, else 16.
+  // Items as the chunk kernels cut them: 128 rows on tcgen05, 64 on
+  // row-owning warps, else 16.
+  const bool umma = umma_chunk_ok(head_size, group, rows);
   const bool row_owning = (head_size == 64 || head_size == 128) && 64 % group == 0 && rows > 32;
-  const int tokens = (row_owning ? 64 : 16) / group;
+  const int tokens = (umma ? 128 : row_owning ? 64 : 16) / group;
   const long long groups = (max_chunk + tokens - 1) / tokens;
   const long long items = (long long)num_seqs * num_kv_heads * groups;
   // Measured on GB300 (bf16, D 128, 32 q / 4 kv heads; 256 sequences of up
   // to 3584 tokens with 2 to 64 tokens a chunk, 8 of up to 8192 and one of
-  // 100,000; consecutive steps): V1 is ahead from 2048 items (13.5 per SM:
-  // 1.23x at 4 tokens, 1.03x at 16, 1.18x at 64), V2 at 1024 items and fewer
-  // (6.7 per SM: 1.02x at 2 tokens, 1.12x at 8).  A chunk item's epilogue
-  // costs more than a decode item's, and V1 pays it once per sequence; the
-  // switch sits between the two measured counts.
-  if (items >= 8LL * sm_count) return 0;
+  // 100,000; consecutive steps).  On the 16- and 64-row kernels V1 is ahead
+  // from 2048 items (13.5 per SM: 1.23x at 4 tokens), V2 at 1024 and fewer
+  // (6.7 per SM: 1.02x at 2 tokens, 1.12x at 8).  On the tcgen05 kernel V1 is
+  // ahead from 1024 items (1.36x at 16 tokens, 1.67x at 64), V2 at 128 and
+  // fewer.  A chunk item's epilogue costs more than a decode item's, and V1
+  // pays it once per sequence; each switch sits between the measured counts.
+  if (items >= (umma ? 4LL : 8LL) * sm_count) return 0;
   return 1;
 }
 

@@ -1,0 +1,623 @@
+// Query chunks on the 5th-generation tensor cores (tcgen05, sm_103a): items
+// of 128 (token, head) rows, D = 128, 16-bit inputs.
+//
+// S = Q.K^T and O += P.V are each a few tcgen05.mma instructions issued by one
+// thread, operands in shared memory (128-byte swizzle, as TMA lands them), the
+// fp32 accumulators in tensor memory:
+//   S[128 rows][64 keys]  = Q[128][D] . K^T          (K-major A and B)
+//   O[128 rows][D]       += P[128][64 keys] . V[64][D] (P K-major, V MN-major)
+// Four softmax warps own one row each per thread (tensor-memory lane = row):
+// a row's maximum and sum need no shuffles.  P is written, rounded to the
+// input type, over the stage's K bytes (dead once S is computed), so a stage
+// is only its K and V.  The running maximum is raised lazily: O is rescaled
+// only when a stage's maximum exceeds the one in use by more than 2^8 in the
+// exponent's units, which is exact (the final normaliser uses the same
+// reference) and leaves the rescale out of almost every stage.
+//
+// Warps: 0-3 softmax and output, 4 producer (TMA of K/V pages, work items),
+// 5 MMA issuer (and the tensor-memory allocation).  Every wait is bounded.
+#include <type_traits>
+
+#include "pa_attn.cuh"
+
+namespace pa {
+namespace {
+
+constexpr int kUmmaRows = 128;        // rows of an item: the MMA's M
+constexpr int kUmmaKeys = 64;         // keys of a stage: the S MMA's N
+constexpr int kUmmaD = 128;           // head size
+constexpr int kUmmaTmemCols = 256;    // S at column 0 (64), O at column 128 (128)
+constexpr int kUmmaStages = 2;
+constexpr int kUmmaPanel = kUmmaKeys * 128;             // one 128-byte panel of a stage's rows
+constexpr int kUmmaHalf = (kUmmaD * 2 / 128) * kUmmaPanel;  // K (or V) bytes of a stage
+constexpr int kUmmaStageBytes = 2 * kUmmaHalf;
+constexpr int kUmmaQPanel = kUmmaRows * 128;
+constexpr int kUmmaQBytes = (kUmmaD * 2 / 128) * kUmmaQPanel;
+constexpr float kLazyMargin = 8.f;    // log2 units
+
+struct UmmaStage {
+  int row0, kvh, part;  // the item: first query row, KV head, partition
+  int tok0;             // key of the stage's first row
+  int valid;            // keys of the stage in the item's range
+  int flags;            // kStage*
+  int rows;             // (token, head) rows of the item
+  int lim_base;         // the item's first token sees keys below lim_base + 1
+};
+
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// The mbarrier completes (one arrival) once every tcgen05 operation this
+// thread issued before has completed.
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   bar)
+               : "memory");
+}
+// D (tensor memory) = A . B (+ D if accumulate), A and B from shared memory.
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                       uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// 32 columns of this warp's 32 lanes (lane = thread), one 32-bit word each;
+// the values may be used only after tmem_ld_wait, which takes them through.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+               : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[32]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31]) :: "memory");
+}
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+               : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor: 128-byte swizzle, start address, leading
+// and stride byte offsets (in 16-byte units, 14 bits each), the sm_100
+// descriptor version (bit 46).
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = (uint64_t)((addr >> 4) & 0x3FFFu);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;  // 128-byte swizzle
+  return d;
+}
+
+// Instruction descriptor of kind::f16: fp32 accumulator, A and B both bf16 (or
+// both f16), A K-major, B K-major or MN-major, M x N.
+template <typename T>
+__host__ __device__ constexpr uint32_t instr_desc(int m, int n, bool b_mn_major) {
+  constexpr uint32_t ab = std::is_same<T, __nv_bfloat16>::value ? 1u : 0u;
+  return (1u << 4) | (ab << 7) | (ab << 10) | ((b_mn_major ? 1u : 0u) << 16) |
+         ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
+}
+
+}  // namespace
+
+template <typename T>
+// two CTAs an SM: at most 168 registers a thread
+__global__ void __launch_bounds__(192, 2)
+    pa_umma_chunk_kernel(const __grid_constant__ AttnParams p,
+                         const __grid_constant__ CUtensorMap tmap_k,
+                         const __grid_constant__ CUtensorMap tmap_v) {
+  constexpr int D = kUmmaD;
+  constexpr int NST = kUmmaStages;
+  constexpr int NPANELS = D * (int)sizeof(T) / 128;
+  constexpr uint32_t kIdescS = instr_desc<T>(kUmmaRows, kUmmaKeys, false);
+  constexpr uint32_t kIdescPV = instr_desc<T>(kUmmaRows, D, true);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t *ring = smem;                                  // NST x [K | V]
+  uint8_t *qbuf = ring + NST * kUmmaStageBytes;          // [panel][128 rows][128 B]
+  UmmaStage *info = reinterpret_cast<UmmaStage *>(qbuf + kUmmaQBytes);
+  uint64_t *bars = reinterpret_cast<uint64_t *>(info + NST);
+  // full[NST], empty[NST], q_full, s_full, p_full, o_done, drain, never
+  volatile int *flags = reinterpret_cast<volatile int *>(bars + 2 * NST + 6);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * NST + 6) + 4;
+  const uint32_t ring_u32 = smem_u32(ring), q_u32 = smem_u32(qbuf);
+  const uint32_t full0 = smem_u32(bars), empty0 = full0 + 8 * NST;
+  const uint32_t q_full = empty0 + 8 * NST, s_full = q_full + 8, p_full = s_full + 8,
+                 o_done = p_full + 8, drain = o_done + 8, never = drain + 8;
+  const uint64_t limit = p.wait_limit_ns;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < NST; ++i) {
+      mbar_init(full0 + 8 * i, 1);
+      mbar_init(empty0 + 8 * i, 1);
+    }
+    mbar_init(q_full, 4);
+    mbar_init(s_full, 1);
+    mbar_init(p_full, 4);
+    mbar_init(o_done, 1);
+    mbar_init(drain, 1);
+    mbar_init(never, 1);
+    flags[0] = 0;
+    fence_mbar_init();
+  }
+  // Launched with programmatic dependent launch: wait for the previous kernel
+  // in the stream before the tensor memory is taken, so that a CTA started
+  // early never holds columns that a still-running CTA of an earlier launch
+  // of this kernel on the same SM is waiting for.
+  pdl_wait_primary();
+  if (warp == 5) {
+    tmem_alloc(smem_u32(tmem_slot), kUmmaTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t tmem_s = tmem, tmem_o = tmem + 128;
+
+  if (warp == 4) {
+    // ======================= producer warp =======================
+    if (lane == 0) {
+      prefetch_tmap(&tmap_k);
+      prefetch_tmap(&tmap_v);
+    }
+    const int U = p.unit_rows;
+    const int G = p.group;
+    int cs = 0, cbase = 0, c_cnt = 0, c_incl = 0, c_L = 0, c_total = 0, c_qs = 0, c_n = 0,
+        c_nrg = 0;
+    bool c_loaded = false;
+    // the running count of items per sequence, 32 sequences at a time:
+    // items are (KV head, partition, row group) of each sequence
+    auto load_chunk = [&]() {
+      const int sl = cs + lane;
+      c_L = 0;
+      c_qs = 0;
+      c_n = 0;
+      if (sl < p.num_seqs) {
+        c_L = __ldg(p.seq_lens + sl);
+        if (c_L < 0 || c_L > p.max_seq_len) {
+          report(p.status, kStatusBadInput);
+          c_L = c_L < 0 ? 0 : p.max_seq_len;
+        }
+        c_qs = __ldg(p.q_start + sl);
+        const int qe = __ldg(p.q_start + sl + 1);
+        c_n = qe - c_qs;
+        if (c_qs < 0 || c_n < 0 || c_n > c_L || qe > p.num_rows) {
+          report(p.status, kStatusBadInput);  // its rows get no items
+          c_n = 0;
+        }
+      }
+      const int c_np = (c_L + p.range_tokens - 1) / p.range_tokens;
+      c_nrg = (c_n + p.chunk_tokens - 1) / p.chunk_tokens;
+      c_cnt = sl < p.num_seqs ? p.num_kv_heads * c_np * c_nrg : 0;
+      c_incl = c_cnt;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, c_incl, off);
+        if (lane >= off) c_incl += t;
+      }
+      c_total = __shfl_sync(0xffffffffu, c_incl, 31);
+      c_loaded = true;
+    };
+    auto grab_issue = [&]() -> int { return atomic_add_lane0(p.sched, lane); };
+    const int takers = (int)gridDim.x;
+    auto grab_value = [&](int raw) -> int { return takers + __shfl_sync(0xffffffffu, raw, 0); };
+    int item = blockIdx.x;
+    int i = 0;  // stages issued
+    bool ok = true;
+    while (true) {
+      int s = 0, kvh = 0, part = 0, L = 0, nrg = 0, qs = 0, n_s = 0, rg = 0;
+      bool found = false;
+      if (item < 0) {
+        if (lane == 0) report(p.status, kStatusBadInput);
+      } else {
+        while (true) {
+          if (!c_loaded) load_chunk();
+          if (item < cbase + c_total) {
+            const unsigned hit = __ballot_sync(0xffffffffu, cbase + c_incl > item);
+            const int ls = __ffs(hit) - 1;
+            s = cs + ls;
+            L = __shfl_sync(0xffffffffu, c_L, ls);
+            nrg = __shfl_sync(0xffffffffu, c_nrg, ls);
+            qs = __shfl_sync(0xffffffffu, c_qs, ls);
+            n_s = __shfl_sync(0xffffffffu, c_n, ls);
+            const int first = cbase + __shfl_sync(0xffffffffu, c_incl - c_cnt, ls);
+            const int np_s = (L + p.range_tokens - 1) / p.range_tokens;
+            const int per_head = np_s * nrg;
+            kvh = (item - first) / per_head;
+            const int rem = (item - first) % per_head;
+            part = rem / nrg;
+            rg = rem % nrg;
+            found = s < p.num_seqs;
+            break;
+          }
+          if (cs + 32 >= p.num_seqs) break;
+          cs += 32;
+          cbase += c_total;
+          c_loaded = false;
+        }
+      }
+      if (!found) break;
+      int next_raw = 0;
+      const int t_first = rg * p.chunk_tokens;
+      const int ntok = min(p.chunk_tokens, n_s - t_first);
+      const int lim_base = L - n_s + t_first;
+      const int row0 = qs + t_first;
+      const int tok_begin = part * p.range_tokens;
+      const int tok_end = min(min(tok_begin + p.range_tokens, L), lim_base + ntok);
+      if (part == 0 && p.row_limit)
+        for (int t = lane; t < ntok; t += 32) p.row_limit[row0 + t] = lim_base + t + 1;
+      if (tok_end <= tok_begin) {  // the partition lies past every token of the group
+        item = grab_value(grab_issue());
+        continue;
+      }
+      // a window of 64 block-table entries (lane j: pages win0 + j and
+      // win0 + 32 + j), slid by 32 pages when a stage reaches the second half
+      const int32_t *bt = p.block_tables + (size_t)s * p.max_blocks_per_seq;
+      const int last_page = (tok_end - 1) >> p.log2_block_size;
+      auto load_entry = [&](int page) -> int {
+        return (page >= 0 && page <= last_page) ? __ldg(bt + page) : -1;
+      };
+      int win0 = tok_begin >> p.log2_block_size;
+      int cur = load_entry(win0 + lane);
+      int nxt = load_entry(win0 + 32 + lane);
+      const int n_st = (tok_end - tok_begin + kUmmaKeys - 1) / kUmmaKeys;
+      for (int j = 0; j < n_st; ++j) {
+        const int st = i % NST;
+        if (i >= NST) {
+          bool w = true;
+          if (lane == 0) w = mbar_wait(empty0 + 8 * st, ((i / NST) - 1) & 1, limit, flags);
+          ok = __shfl_sync(0xffffffffu, w, 0);
+          if (!ok) break;
+        }
+        const int stage_tok0 = tok_begin + j * kUmmaKeys;
+        const int valid = min(kUmmaKeys, tok_end - stage_tok0);
+        const int n_units = (valid + U - 1) / U;
+        const int tok = stage_tok0 + lane * U;
+        const int rel = ((lane < n_units ? tok : stage_tok0) >> p.log2_block_size) - win0;
+        const int a = __shfl_sync(0xffffffffu, cur, rel & 31);
+        const int b = __shfl_sync(0xffffffffu, nxt, rel & 31);
+        int y = -1;
+        if (lane < n_units) {
+          const int blk = rel < 32 ? a : b;
+          if ((unsigned)blk >= (unsigned)p.num_blocks)
+            report(p.status, kStatusBadInput);
+          else
+            y = (blk * p.num_kv_heads + kvh) * p.block_size + (tok & (p.block_size - 1));
+        }
+        const unsigned valid_mask = __ballot_sync(0xffffffffu, y >= 0);
+        if (lane == 0) {
+          UmmaStage &h = info[st];
+          h.row0 = row0;
+          h.kvh = kvh;
+          h.part = part;
+          h.tok0 = stage_tok0;
+          h.valid = valid;
+          h.flags = (j == 0 ? kStageFirst : 0) | (j == n_st - 1 ? kStageLast : 0);
+          h.rows = ntok * G;
+          h.lim_base = lim_base;
+          mbar_arrive_expect_tx(full0 + 8 * st,
+                                (uint32_t)__popc(valid_mask) * U * 128u * NPANELS * 2u);
+        }
+        __syncwarp();
+        if (y >= 0) {
+          // rows lane*U .. of every panel: [panel][64 rows][128 B] per tensor
+          const uint32_t kdst = ring_u32 + (uint32_t)st * kUmmaStageBytes + (uint32_t)(lane * U) * 128u;
+#pragma unroll
+          for (int pn = 0; pn < NPANELS; ++pn) {
+            tma_load_2d(kdst + pn * kUmmaPanel, &tmap_k, pn * 64, y, full0 + 8 * st);
+            tma_load_2d(kdst + kUmmaHalf + pn * kUmmaPanel, &tmap_v, pn * 64, y, full0 + 8 * st);
+          }
+        }
+        if (j == 0) next_raw = grab_issue();
+        ++i;
+        const int next_rel = ((stage_tok0 + kUmmaKeys) >> p.log2_block_size) - win0;
+        if (next_rel >= 32) {
+          cur = nxt;
+          win0 += 32;
+          nxt = load_entry(win0 + 32 + lane);
+        }
+      }
+      if (!ok) break;
+      item = grab_value(next_raw);
+    }
+    pdl_launch_dependents();
+    if (ok) {  // no more items
+      const int st = i % NST;
+      if (i >= NST) {
+        bool w = true;
+        if (lane == 0) w = mbar_wait(empty0 + 8 * st, ((i / NST) - 1) & 1, limit, flags);
+        ok = __shfl_sync(0xffffffffu, w, 0);
+      }
+      if (ok && lane == 0) {
+        info[st].flags = kStageEnd;
+        mbar_arrive(full0 + 8 * st);
+      }
+      if (ok) ++i;
+    }
+    if (!ok && lane == 0) {
+      report(p.status, kStatusTimeout);
+      flags[0] = 1;
+    }
+    if (lane == 0) {  // every copy of this CTA lands before it retires
+      const int first = i > NST ? i - NST : 0;
+      for (int j = first; j < i; ++j)
+        mbar_wait(full0 + 8 * (j % NST), (j / NST) & 1, kDrainLimitNs, nullptr);
+    }
+    __syncwarp();
+  } else if (warp == 5) {
+    // ======================= MMA warp (one thread issues) =======================
+    if (lane == 0) {
+      bool ok = true;
+      int items = 0;
+      for (int i = 0;; ++i) {
+        const int st = i % NST;
+        ok = mbar_wait(full0 + 8 * st, (i / NST) & 1, limit, flags);
+        if (!ok) break;
+        const UmmaStage h = info[st];
+        if (h.flags & kStageEnd) break;
+        if (h.flags & kStageFirst) {
+          ok = mbar_wait(q_full, items & 1, limit, flags);
+          if (!ok) break;
+          ++items;
+        }
+        tc_fence_after();
+        const uint32_t kst = ring_u32 + (uint32_t)st * kUmmaStageBytes;
+        const uint32_t vst = kst + kUmmaHalf;
+        // S = Q K^T: D / 16 k-steps; a k-step is 32 bytes inside a 128-byte
+        // panel of Q (128 rows) and of K (64 rows)
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t koff = (uint32_t)(ks & 3) * 32u;
+          const uint64_t da = smem_desc(q_u32 + (uint32_t)(ks >> 2) * kUmmaQPanel + koff, 16, 1024);
+          const uint64_t db = smem_desc(kst + (uint32_t)(ks >> 2) * kUmmaPanel + koff, 16, 1024);
+          tc_mma(tmem_s, da, db, kIdescS, ks > 0 ? 1u : 0u);
+        }
+        tc_commit(s_full);
+        ok = mbar_wait(p_full, i & 1, limit, flags);
+        if (!ok) break;
+        tc_fence_after();
+        // O += P V: 4 k-steps of 16 keys; P [128 rows][64 keys] over the K
+        // bytes, V MN-major: 64 columns a panel (LBO), 8 keys a 1024-byte
+        // group (SBO)
+#pragma unroll
+        for (int kk = 0; kk < kUmmaKeys / 16; ++kk) {
+          const uint64_t da = smem_desc(kst + (uint32_t)kk * 32u, 16, 1024);
+          const uint64_t db = smem_desc(vst + (uint32_t)kk * 2048u, kUmmaPanel, 1024);
+          tc_mma(tmem_o, da, db, kIdescPV, ((h.flags & kStageFirst) && kk == 0) ? 0u : 1u);
+        }
+        tc_commit(empty0 + 8 * st);  // the stage's K, P and V are read
+        if (h.flags & kStageLast) tc_commit(o_done);
+      }
+      // nothing of this thread's may still run when the memory is freed
+      tc_commit(drain);
+      mbar_wait(drain, 0, kDrainLimitNs, nullptr);
+      if (!ok) {
+        report(p.status, kStatusTimeout);
+        flags[0] = 1;
+      }
+    }
+    __syncwarp();
+  } else {
+    // ======================= softmax warps: thread = row =======================
+    const int r = threadIdx.x;  // 0..127: the row, and its tensor-memory lane
+    const uint32_t lane_off = (uint32_t)(32 * warp) << 16;
+    const int G = p.group;
+    float m_run = -CUDART_INF_F, m_true = -CUDART_INF_F, l = 0.f;
+    int lim = 0;
+    bool ok = true;
+    int items = 0;
+    if (p.debug_flags & kDebugStallConsumers) {
+      // Wait on a barrier that nothing releases: the bound must end it.
+      ok = mbar_wait(never, 0, limit, flags);
+      ok = __all_sync(0xffffffffu, ok);
+    }
+    for (int i = 0; ok; ++i) {
+      const int st = i % NST;
+      const bool w = mbar_wait(full0 + 8 * st, (i / NST) & 1, limit, flags);
+      ok = __all_sync(0xffffffffu, w);
+      if (!ok) break;
+      const UmmaStage h = info[st];
+      if (h.flags & kStageEnd) break;
+      uint8_t *kst = ring + (size_t)st * kUmmaStageBytes;
+      uint8_t *vst = kst + kUmmaHalf;
+      const int orow_tok = r / G, orow_head = h.kvh * G + r % G;
+      if (h.flags & kStageFirst) {
+        // this row's query into the swizzled Q tile (zeros past the item's rows)
+        const bool live = r < h.rows;
+        const uint4 *src = reinterpret_cast<const uint4 *>(
+            static_cast<const T *>(p.query) +
+            ((size_t)(h.row0 + (live ? orow_tok : 0)) * p.num_heads + orow_head) * D);
+#pragma unroll
+        for (int c = 0; c < D / 8; ++c) {
+          const uint4 v = live ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
+          const int pn = c >> 3, cc = c & 7;
+          *reinterpret_cast<uint4 *>(qbuf + pn * kUmmaQPanel + r * 128 + ((cc ^ (r & 7)) << 4)) = v;
+        }
+        lim = live ? h.lim_base + orow_tok + 1 : 0;
+        m_run = -CUDART_INF_F;
+        m_true = -CUDART_INF_F;
+        l = 0.f;
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(q_full);
+      }
+      {
+        const bool w2 = mbar_wait(s_full, i & 1, limit, flags);
+        ok = __all_sync(0xffffffffu, w2);
+        if (!ok) break;
+      }
+      tc_fence_after();
+      uint32_t sa[32], sb[32];
+      tmem_ld32(tmem_s + lane_off, sa);
+      tmem_ld32(tmem_s + lane_off + 32, sb);
+      tmem_ld_wait(sa);
+      tmem_ld_wait(sb);
+      // scores in log2 units; keys past the range or this row's limit: -inf
+      float x[64];
+#pragma unroll
+      for (int k = 0; k < 64; ++k) {
+        const float v = __uint_as_float(k < 32 ? sa[k] : sb[k - 32]) * p.scale_log2;
+        x[k] = (k >= h.valid || h.tok0 + k >= lim) ? -CUDART_INF_F : v;
+      }
+      float mt = -CUDART_INF_F;
+#pragma unroll
+      for (int k = 0; k < 64; ++k) mt = fmaxf(mt, x[k]);
+      m_true = fmaxf(m_true, mt);
+      const bool raise = mt > m_run + kLazyMargin;  // also m_run = -inf and mt finite
+      const float alpha = raise ? exp2f(m_run - mt) : 1.f;  // 0 when m_run = -inf
+      if (raise) m_run = mt;
+      if (!(h.flags & kStageFirst) && __any_sync(0xffffffffu, raise)) {
+        // rescale this row's O (every lane takes part in the warp's loads)
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(tmem_o + lane_off + 32 * c, o);
+          tmem_ld_wait(o);
+#pragma unroll
+          for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
+          tmem_st32(tmem_o + lane_off + 32 * c, o);
+        }
+        tmem_st_wait();
+      }
+      l *= alpha;
+      const float mb = m_run == -CUDART_INF_F ? 0.f : m_run;
+      // P rounded to the input type; the sum adds the rounded values.  Row r
+      // of P [128][64 keys] over the stage's K bytes, 128-byte swizzle.
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        uint32_t w4[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const uint32_t pk = MmaOp<T>::pack(exp2f(x[8 * c + 2 * e] - mb), exp2f(x[8 * c + 2 * e + 1] - mb));
+          const float2 f = MmaOp<T>::unpack(pk);
+          l += f.x + f.y;
+          w4[e] = pk;
+        }
+        *reinterpret_cast<uint4 *>(kst + r * 128 + ((c ^ (r & 7)) << 4)) =
+            make_uint4(w4[0], w4[1], w4[2], w4[3]);
+      }
+      // V rows past the range may hold stale or foreign bytes (0 x NaN would
+      // reach O): zero them
+      if (h.valid < kUmmaKeys) {
+        const int n = (kUmmaKeys - h.valid) * (D * (int)sizeof(T) / 16);
+        for (int idx = r; idx < n; idx += 128) {
+          const int row = h.valid + idx / (D * (int)sizeof(T) / 16);
+          const int c = idx % (D * (int)sizeof(T) / 16);
+          *reinterpret_cast<uint4 *>(vst + (c >> 3) * kUmmaPanel + row * 128 + (((c & 7) ^ (row & 7)) << 4)) =
+              make_uint4(0u, 0u, 0u, 0u);
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(p_full);
+      if (h.flags & kStageLast) {
+        const bool w3 = mbar_wait(o_done, items & 1, limit, flags);
+        ok = __all_sync(0xffffffffu, w3);
+        if (!ok) break;
+        ++items;
+        tc_fence_after();
+        // O is relative to m_run; the record takes the true maximum
+        const float lt = m_true == -CUDART_INF_F ? 0.f : l * exp2f(m_run - m_true);
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        const bool live = r < h.rows;
+        const size_t orow = ((size_t)h.row0 + orow_tok) * p.num_heads + orow_head;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(tmem_o + lane_off + 32 * c, o);
+          tmem_ld_wait(o);
+          if (!live) continue;
+          if (p.write_partials) {
+            float *dst = p.tmp_out + (orow * p.max_parts + h.part) * D + 32 * c;
+#pragma unroll
+            for (int k = 0; k < 32; k += 4)
+              *reinterpret_cast<float4 *>(dst + k) =
+                  make_float4(__uint_as_float(o[k]) * inv, __uint_as_float(o[k + 1]) * inv,
+                              __uint_as_float(o[k + 2]) * inv, __uint_as_float(o[k + 3]) * inv);
+          } else {
+            T *dst = static_cast<T *>(p.out) + orow * D + 32 * c;
+#pragma unroll
+            for (int k = 0; k < 32; k += 8) {
+              uint4 v;
+              v.x = MmaOp<T>::pack(__uint_as_float(o[k]) * inv, __uint_as_float(o[k + 1]) * inv);
+              v.y = MmaOp<T>::pack(__uint_as_float(o[k + 2]) * inv, __uint_as_float(o[k + 3]) * inv);
+              v.z = MmaOp<T>::pack(__uint_as_float(o[k + 4]) * inv, __uint_as_float(o[k + 5]) * inv);
+              v.w = MmaOp<T>::pack(__uint_as_float(o[k + 6]) * inv, __uint_as_float(o[k + 7]) * inv);
+              *reinterpret_cast<uint4 *>(dst + k) = v;
+            }
+          }
+        }
+        if (live && p.write_partials) {
+          const size_t prow = orow * p.max_parts + h.part;
+          p.max_logits[prow] = m_true * 0.69314718055994530942f;  // natural-log units
+          p.exp_sums[prow] = lt;
+        }
+        tc_fence_before();
+      }
+    }
+    if (!ok && lane == 0) {
+      report(p.status, kStatusTimeout);
+      flags[0] = 1;
+    }
+    pdl_launch_dependents();
+  }
+
+  // every role is done with the tensor memory: free it
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kUmmaTmemCols);
+  }
+  if (!p.sched_reset_later) {
+    if (threadIdx.x == 0) {
+      __threadfence();
+      if (atomicAdd(p.sched + 1, 1) == (int)gridDim.x - 1) {
+        atomicExch(p.sched, 0);
+        atomicExch(p.sched + 1, 0);
+      }
+    }
+  }
+}
+
+size_t umma_chunk_smem_bytes() {
+  return 1024 + (size_t)kUmmaStages * kUmmaStageBytes + kUmmaQBytes +
+         kUmmaStages * sizeof(UmmaStage) + (2 * kUmmaStages + 6) * 8 + 32;
+}
+
+AttnKernelInfo attn_kernel_umma_chunk(int dtype_bf16) {
+  AttnKernelInfo k{};
+  k.fn = dtype_bf16 ? reinterpret_cast<const void *>(&pa_umma_chunk_kernel<__nv_bfloat16>)
+                    : reinterpret_cast<const void *>(&pa_umma_chunk_kernel<__half>);
+  k.consumer_warps = 5;  // 4 softmax warps and the MMA warp; the producer is the sixth
+  k.stage_tokens = kUmmaKeys;
+  k.max_group = kUmmaRows;
+  k.umma = 1;
+  return k;
+}
+
+}  // namespace pa

@@ -89,7 +89,18 @@ struct AttnKernelInfo {
   int stage_tokens;   // tokens of one ring stage
                       // (consumer_warps * kTileTokens, or 64 for row-owning warps)
   int max_group;      // largest H / Hkv it handles (query chunks: rows of an item)
+  int umma;           // 1: the tcgen05 query-chunk kernel (its own layout and launch)
 };
+
+// Query chunks on tcgen05: D 128, 16-bit, at least one full 128-row item per
+// KV head.
+inline bool umma_chunk_ok(int head_size, int group, long long max_rows) {
+  return head_size == 128 && group >= 1 && 128 % group == 0 && max_rows >= 128;
+}
+AttnKernelInfo attn_kernel_umma_chunk(int dtype_bf16);
+size_t umma_chunk_smem_bytes();
+constexpr int kUmmaStagesHost = 2;
+constexpr int kUmmaTmemColsHost = 256;  // tensor-memory columns per CTA (of 512 per SM)
 
 // Dynamic shared memory the attention kernel needs for `stages` stages (the
 // kernel's carve-up, in order: the ring of stages, each its K and V bytes and

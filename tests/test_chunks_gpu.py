@@ -2,7 +2,9 @@
 oracle's query_chunks, element by element: chunks of the last n tokens of
 each sequence, causal among themselves, over V1 / V2 / auto, every tensor
 dtype, head size and a spread of group sizes (which set how many chunk
-tokens an item holds: 16 / G)."""
+tokens an item holds: 16 / G on the two-n-tile kernel, 64 / G on the
+row-owning one, 128 / G on the tcgen05 one, which takes chunks of at least
+128 rows per KV head at D 128)."""
 import pytest
 import torch
 
@@ -32,6 +34,11 @@ CASES = [  # dtype, D, G, Hkv, bs, P, lens, qlens
     (torch.bfloat16, 256, 2, 2, 32, 512, [3000, 1200], [12, 8]),
     (torch.float16, 128, 1, 8, 16, 512, [2500, 600, 17], [20, 3, 17]),  # 16 tokens an item
     (torch.bfloat16, 64, 16, 1, 64, 256, [5000, 260], [2, 1]),           # one token an item
+    # tcgen05 kernel (>= 128 rows per KV head at D 128): f16, pages of 32, 8 and 64 tokens,
+    # a chunk that is its whole sequence, ragged row groups
+    (torch.float16, 128, 4, 2, 32, 512, [1000, 2100, 70], [40, 64, 70]),
+    (torch.bfloat16, 128, 16, 1, 8, 256, [600, 1300], [9, 13]),
+    (torch.bfloat16, 128, 2, 4, 64, 512, [3000, 129], [64, 129]),
 ]
 
 
@@ -55,6 +62,29 @@ def test_chunks_match_oracle(dtype, D, G, Hkv, bs, P, lens, qlens, variant):
                              max_chunk=max(qlens), variant=variant)
         assert pa.pa_read_device_status(ws) == pa.PA_OK
         assert_close(out, ref, dtype, f"chunks v{variant}")
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16], ids=["bf16", "f16"])
+def test_tcgen05_and_mma_sync_kernels_agree_with_the_oracle(dtype):
+    """The same chunks (136 and 264 rows per KV head) on the tcgen05 kernel and,
+    with PA_DEBUG_NO_TCGEN05, on the row-owning mma.sync kernel: both within
+    the bar of the oracle, V1 and V2."""
+    H, Hkv, D, P = 16, 2, 128, 256
+    c, q, qs = _chunk_case(4242, [700, 1800, 40, 2500], [17, 33, 40, 1], H, Hkv, D, dtype, 16, P)
+    ref = oracle.query_chunks(q, c.key_cache, c.value_cache, c.block_tables, c.seq_lens, qs,
+                              c.scale)
+    dev = "cuda"
+    R = q.shape[0]
+    ws = pa.alloc_workspace(R, H, D, c.max_seq_len, P)
+    args = (q.to(dev), c.key_cache.to(dev), c.value_cache.to(dev), c.block_tables.to(dev),
+            c.seq_lens.to(dev), qs.to(dev))
+    for flags in (0, pa.PA_DEBUG_NO_TCGEN05):
+        for variant in (pa.PA_VARIANT_V1, pa.PA_VARIANT_V2):
+            out = torch.full((R, H, D), float("nan"), dtype=dtype, device=dev)
+            pa.pa_chunks_forward(out, *args, c.scale, P, ws, max_seq_len=c.max_seq_len,
+                                 max_chunk=40, variant=variant, debug_flags=flags)
+            assert pa.pa_read_device_status(ws) == pa.PA_OK
+            assert_close(out, ref, dtype, f"chunks flags {flags} v{variant}")
 
 
 def test_single_token_chunks_equal_decode():
@@ -127,7 +157,7 @@ def test_bench_chunk_workload_full_size():
 def test_long_chunk_workload_full_size():
     """Long chunks at full size: the c4_batch256 cache with a 64-token causal
     chunk per sequence (16384 query rows, 512 (token, head) rows per KV head,
-    run as 64-row items on row-owning warps), V2 and V1, every output
+    run as 128-row items on the tcgen05 kernel), V2 and V1, every output
     against the oracle; the benchmark's `long_chunks` entry runs this step."""
     c = workloads.config_case("c4_batch256")
     q, qs = workloads.chunk_queries(c, 64)
