@@ -26,7 +26,7 @@ namespace {
 constexpr int kUmmaRows = 128;        // rows of an item: the MMA's M
 constexpr int kUmmaKeys = 64;         // keys of a stage: the S MMA's N
 constexpr int kUmmaD = 128;           // head size
-constexpr int kUmmaTmemCols = 256;    // S at column 0 (64), O at column 128 (128)
+constexpr int kUmmaTmemCols = 256;    // S at columns 0 and 64 (two buffers), O at 128
 constexpr int kUmmaStages = 2;
 constexpr int kUmmaPanel = kUmmaKeys * 128;             // one 128-byte panel of a stage's rows
 constexpr int kUmmaHalf = (kUmmaD * 2 / 128) * kUmmaPanel;  // K (or V) bytes of a stage
@@ -92,6 +92,12 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
   asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
                : "memory");
 }
+// 2^x on the special-function unit (flushes subnormal results to zero; 2^-inf = 0)
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 __device__ __forceinline__ void tmem_st_wait() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
@@ -139,12 +145,12 @@ __global__ void __launch_bounds__(192, 2)
   uint8_t *qbuf = ring + NST * kUmmaStageBytes;          // [panel][128 rows][128 B]
   UmmaStage *info = reinterpret_cast<UmmaStage *>(qbuf + kUmmaQBytes);
   uint64_t *bars = reinterpret_cast<uint64_t *>(info + NST);
-  // full[NST], empty[NST], q_full, s_full, p_full, o_done, drain, never
-  volatile int *flags = reinterpret_cast<volatile int *>(bars + 2 * NST + 6);
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * NST + 6) + 4;
+  // full[NST], empty[NST], q_full, s_full[2], p_full, o_done, drain, never
+  volatile int *flags = reinterpret_cast<volatile int *>(bars + 2 * NST + 7);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * NST + 7) + 4;
   const uint32_t ring_u32 = smem_u32(ring), q_u32 = smem_u32(qbuf);
   const uint32_t full0 = smem_u32(bars), empty0 = full0 + 8 * NST;
-  const uint32_t q_full = empty0 + 8 * NST, s_full = q_full + 8, p_full = s_full + 8,
+  const uint32_t q_full = empty0 + 8 * NST, s_full = q_full + 8, p_full = s_full + 16,
                  o_done = p_full + 8, drain = o_done + 8, never = drain + 8;
   const uint64_t limit = p.wait_limit_ns;
 
@@ -155,6 +161,7 @@ __global__ void __launch_bounds__(192, 2)
     }
     mbar_init(q_full, 4);
     mbar_init(s_full, 1);
+    mbar_init(s_full + 8, 1);
     mbar_init(p_full, 4);
     mbar_init(o_done, 1);
     mbar_init(drain, 1);
@@ -372,36 +379,60 @@ __global__ void __launch_bounds__(192, 2)
     if (lane == 0) {
       bool ok = true;
       int items = 0;
-      for (int i = 0;; ++i) {
-        const int st = i % NST;
-        ok = mbar_wait(full0 + 8 * st, (i / NST) & 1, limit, flags);
-        if (!ok) break;
-        const UmmaStage h = info[st];
-        if (h.flags & kStageEnd) break;
-        if (h.flags & kStageFirst) {
-          ok = mbar_wait(q_full, items & 1, limit, flags);
-          if (!ok) break;
-          ++items;
-        }
-        tc_fence_after();
+      // S = Q K^T of stage `st` into S buffer b: D / 16 k-steps; a k-step is
+      // 32 bytes inside a 128-byte panel of Q (128 rows) and of K (64 rows)
+      auto issue_s = [&](int st, int b) {
         const uint32_t kst = ring_u32 + (uint32_t)st * kUmmaStageBytes;
-        const uint32_t vst = kst + kUmmaHalf;
-        // S = Q K^T: D / 16 k-steps; a k-step is 32 bytes inside a 128-byte
-        // panel of Q (128 rows) and of K (64 rows)
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
           const uint32_t koff = (uint32_t)(ks & 3) * 32u;
           const uint64_t da = smem_desc(q_u32 + (uint32_t)(ks >> 2) * kUmmaQPanel + koff, 16, 1024);
           const uint64_t db = smem_desc(kst + (uint32_t)(ks >> 2) * kUmmaPanel + koff, 16, 1024);
-          tc_mma(tmem_s, da, db, kIdescS, ks > 0 ? 1u : 0u);
+          tc_mma(tmem_s + 64u * (uint32_t)b, da, db, kIdescS, ks > 0 ? 1u : 0u);
         }
-        tc_commit(s_full);
+        tc_commit(s_full + 8u * (uint32_t)b);
+      };
+      // The S of stage i + 1 is issued before the PV of stage i (its buffer
+      // was read by the softmax of stage i - 1, whose P the PV of i - 1
+      // waited for), so the tensor cores compute it while the softmax warps
+      // work on stage i; within an item only, since a new item's S needs its
+      // queries, which the softmax warps store after the item before ends.
+      UmmaStage h{};
+      ok = mbar_wait(full0, 0, limit, flags);
+      if (ok) h = info[0];
+      bool more = ok && !(h.flags & kStageEnd);
+      if (more) {
+        ok = mbar_wait(q_full, 0, limit, flags);
+        items = 1;
+        if (ok) {
+          tc_fence_after();
+          issue_s(0, 0);
+        }
+        more = ok;
+      }
+      for (int i = 0; more; ++i) {
+        const int st = i % NST, st1 = (i + 1) % NST;
+        const uint32_t par1 = ((i + 1) / NST) & 1;
+        // the next stage's S goes first only if its bytes are already here:
+        // the PV of this stage never waits for the next stage's copies
+        bool s1 = false;
+        UmmaStage h1{};
+        if (mbar_test(full0 + 8 * st1, par1)) {
+          h1 = info[st1];
+          if (!(h1.flags & (kStageEnd | kStageFirst))) {
+            tc_fence_after();
+            issue_s(st1, (i + 1) & 1);
+            s1 = true;
+          }
+        }
         ok = mbar_wait(p_full, i & 1, limit, flags);
         if (!ok) break;
         tc_fence_after();
         // O += P V: 4 k-steps of 16 keys; P [128 rows][64 keys] over the K
         // bytes, V MN-major: 64 columns a panel (LBO), 8 keys a 1024-byte
         // group (SBO)
+        const uint32_t kst = ring_u32 + (uint32_t)st * kUmmaStageBytes;
+        const uint32_t vst = kst + kUmmaHalf;
 #pragma unroll
         for (int kk = 0; kk < kUmmaKeys / 16; ++kk) {
           const uint64_t da = smem_desc(kst + (uint32_t)kk * 32u, 16, 1024);
@@ -410,6 +441,20 @@ __global__ void __launch_bounds__(192, 2)
         }
         tc_commit(empty0 + 8 * st);  // the stage's K, P and V are read
         if (h.flags & kStageLast) tc_commit(o_done);
+        if (!s1) {
+          ok = mbar_wait(full0 + 8 * st1, par1, limit, flags);
+          if (!ok) break;
+          h1 = info[st1];
+          if (h1.flags & kStageEnd) break;
+          if (h1.flags & kStageFirst) {
+            ok = mbar_wait(q_full, items & 1, limit, flags);
+            if (!ok) break;
+            ++items;
+          }
+          tc_fence_after();
+          issue_s(st1, (i + 1) & 1);
+        }
+        h = h1;
       }
       // nothing of this thread's may still run when the memory is freed
       tc_commit(drain);
@@ -465,14 +510,15 @@ __global__ void __launch_bounds__(192, 2)
         if (lane == 0) mbar_arrive(q_full);
       }
       {
-        const bool w2 = mbar_wait(s_full, i & 1, limit, flags);
+        const bool w2 = mbar_wait(s_full + 8 * (i & 1), (i >> 1) & 1, limit, flags);
         ok = __all_sync(0xffffffffu, w2);
         if (!ok) break;
       }
       tc_fence_after();
       uint32_t sa[32], sb[32];
-      tmem_ld32(tmem_s + lane_off, sa);
-      tmem_ld32(tmem_s + lane_off + 32, sb);
+      const uint32_t sbuf = tmem_s + 64u * (uint32_t)(i & 1) + lane_off;
+      tmem_ld32(sbuf, sa);
+      tmem_ld32(sbuf + 32, sb);
       tmem_ld_wait(sa);
       tmem_ld_wait(sb);
       // scores in log2 units; keys past the range or this row's limit: -inf
@@ -490,7 +536,16 @@ __global__ void __launch_bounds__(192, 2)
       const float alpha = raise ? exp2f(m_run - mt) : 1.f;  // 0 when m_run = -inf
       if (raise) m_run = mt;
       if (!(h.flags & kStageFirst) && __any_sync(0xffffffffu, raise)) {
-        // rescale this row's O (every lane takes part in the warp's loads)
+        // rescale this row's O (every lane takes part in the warp's loads),
+        // once the PV of the stage before has completed: its commit
+        // released that stage's slot
+        {
+          const int ip = i - 1;
+          const bool w4 = mbar_wait(empty0 + 8 * (ip % NST), (ip / NST) & 1, limit, flags);
+          ok = __all_sync(0xffffffffu, w4);
+          if (!ok) break;
+        }
+        tc_fence_after();
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t o[32];
@@ -511,7 +566,7 @@ __global__ void __launch_bounds__(192, 2)
         uint32_t w4[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const uint32_t pk = MmaOp<T>::pack(exp2f(x[8 * c + 2 * e] - mb), exp2f(x[8 * c + 2 * e + 1] - mb));
+          const uint32_t pk = MmaOp<T>::pack(ex2(x[8 * c + 2 * e] - mb), ex2(x[8 * c + 2 * e + 1] - mb));
           const float2 f = MmaOp<T>::unpack(pk);
           l += f.x + f.y;
           w4[e] = pk;
@@ -606,7 +661,7 @@ __global__ void __launch_bounds__(192, 2)
 
 size_t umma_chunk_smem_bytes() {
   return 1024 + (size_t)kUmmaStages * kUmmaStageBytes + kUmmaQBytes +
-         kUmmaStages * sizeof(UmmaStage) + (2 * kUmmaStages + 6) * 8 + 32;
+         kUmmaStages * sizeof(UmmaStage) + (2 * kUmmaStages + 7) * 8 + 32;
 }
 
 AttnKernelInfo attn_kernel_umma_chunk(int dtype_bf16) {
