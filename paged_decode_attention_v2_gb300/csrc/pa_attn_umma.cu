@@ -521,16 +521,25 @@ __global__ void __launch_bounds__(192, 2)
       tmem_ld32(sbuf + 32, sb);
       tmem_ld_wait(sa);
       tmem_ld_wait(sb);
-      // scores in log2 units; keys past the range or this row's limit: -inf
+      // scores in log2 units; keys past the range or this row's limit
+      // (key index kvis and up) get -inf, a step every row of the warp skips
+      // when all of them see the whole stage
       float x[64];
 #pragma unroll
-      for (int k = 0; k < 64; ++k) {
-        const float v = __uint_as_float(k < 32 ? sa[k] : sb[k - 32]) * p.scale_log2;
-        x[k] = (k >= h.valid || h.tok0 + k >= lim) ? -CUDART_INF_F : v;
-      }
-      float mt = -CUDART_INF_F;
+      for (int k = 0; k < 64; ++k) x[k] = __uint_as_float(k < 32 ? sa[k] : sb[k - 32]) * p.scale_log2;
+      const int kvis = min(h.valid, lim - h.tok0);
+      if (!__all_sync(0xffffffffu, kvis >= kUmmaKeys)) {
 #pragma unroll
-      for (int k = 0; k < 64; ++k) mt = fmaxf(mt, x[k]);
+        for (int k = 0; k < 64; ++k)
+          if (k >= kvis) x[k] = -CUDART_INF_F;
+      }
+      float m8[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) m8[j] = x[j];
+#pragma unroll
+      for (int k = 8; k < 64; ++k) m8[k & 7] = fmaxf(m8[k & 7], x[k]);
+      const float mt = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                             fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
       m_true = fmaxf(m_true, mt);
       const bool raise = mt > m_run + kLazyMargin;  // also m_run = -inf and mt finite
       const float alpha = raise ? exp2f(m_run - mt) : 1.f;  // 0 when m_run = -inf
@@ -559,8 +568,10 @@ __global__ void __launch_bounds__(192, 2)
       }
       l *= alpha;
       const float mb = m_run == -CUDART_INF_F ? 0.f : m_run;
-      // P rounded to the input type; the sum adds the rounded values.  Row r
-      // of P [128][64 keys] over the stage's K bytes, 128-byte swizzle.
+      // P rounded to the input type; the sum adds the rounded values (four
+      // partial sums).  Row r of P [128][64 keys] over the stage's K bytes,
+      // 128-byte swizzle.
+      float l4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int c = 0; c < 8; ++c) {
         uint32_t w4[4];
@@ -568,12 +579,13 @@ __global__ void __launch_bounds__(192, 2)
         for (int e = 0; e < 4; ++e) {
           const uint32_t pk = MmaOp<T>::pack(ex2(x[8 * c + 2 * e] - mb), ex2(x[8 * c + 2 * e + 1] - mb));
           const float2 f = MmaOp<T>::unpack(pk);
-          l += f.x + f.y;
+          l4[e] += f.x + f.y;
           w4[e] = pk;
         }
         *reinterpret_cast<uint4 *>(kst + r * 128 + ((c ^ (r & 7)) << 4)) =
             make_uint4(w4[0], w4[1], w4[2], w4[3]);
       }
+      l += (l4[0] + l4[1]) + (l4[2] + l4[3]);
       // V rows past the range may hold stale or foreign bytes (0 x NaN would
       // reach O): zero them
       if (h.valid < kUmmaKeys) {
