@@ -92,6 +92,12 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
   asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
                : "memory");
 }
+// max(a, b, c) in one instruction
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
 // 2^x on the special-function unit (flushes subnormal results to zero; 2^-inf = 0)
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -145,13 +151,17 @@ __global__ void __launch_bounds__(192, 2)
   uint8_t *qbuf = ring + NST * kUmmaStageBytes;          // [panel][128 rows][128 B]
   UmmaStage *info = reinterpret_cast<UmmaStage *>(qbuf + kUmmaQBytes);
   uint64_t *bars = reinterpret_cast<uint64_t *>(info + NST);
-  // full[NST], empty[NST], q_full, s_full[2], p_full, o_done, drain, never
-  volatile int *flags = reinterpret_cast<volatile int *>(bars + 2 * NST + 7);
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * NST + 7) + 4;
+  // full[NST], empty[NST], q_full, s_full[2], p_full[2], o_done, drain, never.
+  // S and P barriers come in pairs (stage parity): the softmax may run one
+  // stage ahead of the MMA thread's wait for its P (the next S is issued
+  // before this PV), and one barrier for every stage would then complete
+  // twice before that wait and never show the awaited phase.
+  volatile int *flags = reinterpret_cast<volatile int *>(bars + 2 * NST + 8);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * NST + 8) + 4;
   const uint32_t ring_u32 = smem_u32(ring), q_u32 = smem_u32(qbuf);
   const uint32_t full0 = smem_u32(bars), empty0 = full0 + 8 * NST;
   const uint32_t q_full = empty0 + 8 * NST, s_full = q_full + 8, p_full = s_full + 16,
-                 o_done = p_full + 8, drain = o_done + 8, never = drain + 8;
+                 o_done = p_full + 16, drain = o_done + 8, never = drain + 8;
   const uint64_t limit = p.wait_limit_ns;
 
   if (threadIdx.x == 0) {
@@ -163,6 +173,7 @@ __global__ void __launch_bounds__(192, 2)
     mbar_init(s_full, 1);
     mbar_init(s_full + 8, 1);
     mbar_init(p_full, 4);
+    mbar_init(p_full + 8, 4);
     mbar_init(o_done, 1);
     mbar_init(drain, 1);
     mbar_init(never, 1);
@@ -425,7 +436,7 @@ __global__ void __launch_bounds__(192, 2)
             s1 = true;
           }
         }
-        ok = mbar_wait(p_full, i & 1, limit, flags);
+        ok = mbar_wait(p_full + 8 * (i & 1), (i >> 1) & 1, limit, flags);
         if (!ok) break;
         tc_fence_after();
         // O += P V: 4 k-steps of 16 keys; P [128 rows][64 keys] over the K
@@ -533,13 +544,15 @@ __global__ void __launch_bounds__(192, 2)
         for (int k = 0; k < 64; ++k)
           if (k >= kvis) x[k] = -CUDART_INF_F;
       }
+      // the row maximum: 8 chains of three-input maxima over 8 keys each
       float m8[8];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) m8[j] = x[j];
-#pragma unroll
-      for (int k = 8; k < 64; ++k) m8[k & 7] = fmaxf(m8[k & 7], x[k]);
-      const float mt = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                             fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+      for (int j = 0; j < 8; ++j) {
+        const float *v = x + 8 * j;
+        m8[j] = fmax3(fmax3(v[0], v[1], v[2]), fmax3(v[3], v[4], v[5]), fmaxf(v[6], v[7]));
+      }
+      const float mt = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]),
+                             fmaxf(m8[6], m8[7]));
       m_true = fmaxf(m_true, mt);
       const bool raise = mt > m_run + kLazyMargin;  // also m_run = -inf and mt finite
       const float alpha = raise ? exp2f(m_run - mt) : 1.f;  // 0 when m_run = -inf
@@ -568,8 +581,10 @@ __global__ void __launch_bounds__(192, 2)
       }
       l *= alpha;
       const float mb = m_run == -CUDART_INF_F ? 0.f : m_run;
-      // P rounded to the input type; the sum adds the rounded values (four
-      // partial sums).  Row r of P [128][64 keys] over the stage's K bytes,
+      // P rounded to the input type for the PV product; the row sum adds the
+      // fp32 exponentials (four partial sums), so that no rounded pair needs
+      // unpacking: the two differ by the rounding of P, about 2^-9 relative
+      // and unbiased.  Row r of P [128][64 keys] over the stage's K bytes,
       // 128-byte swizzle.
       float l4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -577,10 +592,9 @@ __global__ void __launch_bounds__(192, 2)
         uint32_t w4[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const uint32_t pk = MmaOp<T>::pack(ex2(x[8 * c + 2 * e] - mb), ex2(x[8 * c + 2 * e + 1] - mb));
-          const float2 f = MmaOp<T>::unpack(pk);
-          l4[e] += f.x + f.y;
-          w4[e] = pk;
+          const float p0 = ex2(x[8 * c + 2 * e] - mb), p1 = ex2(x[8 * c + 2 * e + 1] - mb);
+          l4[e] += p0 + p1;
+          w4[e] = MmaOp<T>::pack(p0, p1);
         }
         *reinterpret_cast<uint4 *>(kst + r * 128 + ((c ^ (r & 7)) << 4)) =
             make_uint4(w4[0], w4[1], w4[2], w4[3]);
@@ -600,7 +614,7 @@ __global__ void __launch_bounds__(192, 2)
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(p_full);
+      if (lane == 0) mbar_arrive(p_full + 8 * (i & 1));
       if (h.flags & kStageLast) {
         const bool w3 = mbar_wait(o_done, items & 1, limit, flags);
         ok = __all_sync(0xffffffffu, w3);
@@ -673,7 +687,7 @@ __global__ void __launch_bounds__(192, 2)
 
 size_t umma_chunk_smem_bytes() {
   return 1024 + (size_t)kUmmaStages * kUmmaStageBytes + kUmmaQBytes +
-         kUmmaStages * sizeof(UmmaStage) + (2 * kUmmaStages + 7) * 8 + 32;
+         kUmmaStages * sizeof(UmmaStage) + (2 * kUmmaStages + 8) * 8 + 32;
 }
 
 AttnKernelInfo attn_kernel_umma_chunk(int dtype_bf16) {
