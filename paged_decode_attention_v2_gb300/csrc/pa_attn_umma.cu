@@ -27,10 +27,13 @@ constexpr int kUmmaRows = 128;        // rows of an item: the MMA's M
 constexpr int kUmmaKeys = 64;         // keys of a stage: the S MMA's N
 constexpr int kUmmaD = 128;           // head size
 constexpr int kUmmaTmemCols = 256;    // S at columns 0 and 64 (two buffers), O at 128
-constexpr int kUmmaStages = 2;
+// K and V of a stage live in separate rings: three K slots (a stage's P is
+// written over its K, so a K slot is busy until the stage's PV), two V slots.
+// K of stage i + 1 then loads while stage i - 1's PV runs.
+constexpr int kUmmaKSlots = 3;
+constexpr int kUmmaVSlots = 2;
 constexpr int kUmmaPanel = kUmmaKeys * 128;             // one 128-byte panel of a stage's rows
 constexpr int kUmmaHalf = (kUmmaD * 2 / 128) * kUmmaPanel;  // K (or V) bytes of a stage
-constexpr int kUmmaStageBytes = 2 * kUmmaHalf;
 constexpr int kUmmaQPanel = kUmmaRows * 128;
 constexpr int kUmmaQBytes = (kUmmaD * 2 / 128) * kUmmaQPanel;
 constexpr float kLazyMargin = 8.f;    // log2 units
@@ -138,36 +141,49 @@ __global__ void __launch_bounds__(192, 2)
                          const __grid_constant__ CUtensorMap tmap_k,
                          const __grid_constant__ CUtensorMap tmap_v) {
   constexpr int D = kUmmaD;
-  constexpr int NST = kUmmaStages;
+  constexpr int NK = kUmmaKSlots, NV = kUmmaVSlots;
   constexpr int NPANELS = D * (int)sizeof(T) / 128;
   constexpr uint32_t kIdescS = instr_desc<T>(kUmmaRows, kUmmaKeys, false);
   constexpr uint32_t kIdescPV = instr_desc<T>(kUmmaRows, D, true);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // The 128-byte swizzle needs every tile 1024-byte aligned.  Two CTAs of
+  // this kernel fit on an SM only without alignment slack, so the kernel
+  // relies on the dynamic shared memory starting 1024-byte aligned (it
+  // starts right after the 1 KB the system reserves) and checks it.
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  uint8_t *smem = reinterpret_cast<uint8_t *>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t *ring = smem;                                  // NST x [K | V]
-  uint8_t *qbuf = ring + NST * kUmmaStageBytes;          // [panel][128 rows][128 B]
-  UmmaStage *info = reinterpret_cast<UmmaStage *>(qbuf + kUmmaQBytes);
-  uint64_t *bars = reinterpret_cast<uint64_t *>(info + NST);
-  // full[NST], empty[NST], q_full, s_full[2], p_full[2], o_done, drain, never.
-  // S and P barriers come in pairs (stage parity): the softmax may run one
-  // stage ahead of the MMA thread's wait for its P (the next S is issued
-  // before this PV), and one barrier for every stage would then complete
-  // twice before that wait and never show the awaited phase.
-  volatile int *flags = reinterpret_cast<volatile int *>(bars + 2 * NST + 8);
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * NST + 8) + 4;
-  const uint32_t ring_u32 = smem_u32(ring), q_u32 = smem_u32(qbuf);
-  const uint32_t full0 = smem_u32(bars), empty0 = full0 + 8 * NST;
-  const uint32_t q_full = empty0 + 8 * NST, s_full = q_full + 8, p_full = s_full + 16,
+  if (smem_u32(smem_raw) & 1023u) {
+    if (threadIdx.x == 0) report(p.status, kStatusBadInput);
+    return;
+  }
+  uint8_t *kring = smem_raw;                             // NK x K: [panel][64 keys][128 B]
+  uint8_t *vring = kring + NK * kUmmaHalf;               // NV x V, the same layout
+  uint8_t *qbuf = vring + NV * kUmmaHalf;                // [panel][128 rows][128 B]
+  UmmaStage *info = reinterpret_cast<UmmaStage *>(qbuf + kUmmaQBytes);  // per K slot
+  uint64_t *bars = reinterpret_cast<uint64_t *>(info + NK);
+  // fullK[NK], emptyK[NK], fullV[NV], emptyV[NV], q_full, s_full[2], p_full[2],
+  // o_done, drain, never.  S and P barriers come in pairs (stage parity): the
+  // softmax may run one stage ahead of the MMA thread's wait for its P (the
+  // next S is issued before this PV), and one barrier for every stage would
+  // then complete twice before that wait and never show the awaited phase.
+  constexpr int NBARS = 2 * NK + 2 * NV + 8;
+  volatile int *flags = reinterpret_cast<volatile int *>(bars + NBARS);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + NBARS) + 4;
+  const uint32_t kring_u32 = smem_u32(kring), vring_u32 = smem_u32(vring), q_u32 = smem_u32(qbuf);
+  const uint32_t fullk0 = smem_u32(bars), emptyk0 = fullk0 + 8 * NK;
+  const uint32_t fullv0 = emptyk0 + 8 * NK, emptyv0 = fullv0 + 8 * NV;
+  const uint32_t q_full = emptyv0 + 8 * NV, s_full = q_full + 8, p_full = s_full + 16,
                  o_done = p_full + 16, drain = o_done + 8, never = drain + 8;
   const uint64_t limit = p.wait_limit_ns;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < NST; ++i) {
-      mbar_init(full0 + 8 * i, 1);
-      mbar_init(empty0 + 8 * i, 1);
+    for (int i = 0; i < NK; ++i) {
+      mbar_init(fullk0 + 8 * i, 1);
+      mbar_init(emptyk0 + 8 * i, 1);
+    }
+    for (int i = 0; i < NV; ++i) {
+      mbar_init(fullv0 + 8 * i, 1);
+      mbar_init(emptyv0 + 8 * i, 1);
     }
     mbar_init(q_full, 4);
     mbar_init(s_full, 1);
@@ -243,7 +259,8 @@ __global__ void __launch_bounds__(192, 2)
     const int takers = (int)gridDim.x;
     auto grab_value = [&](int raw) -> int { return takers + __shfl_sync(0xffffffffu, raw, 0); };
     int item = blockIdx.x;
-    int i = 0;  // stages issued
+    int i = 0;           // stages issued
+    int ik = 0, iv = 0;  // stages whose K (with the end marker) and V copies are issued
     bool ok = true;
     while (true) {
       int s = 0, kvh = 0, part = 0, L = 0, nrg = 0, qs = 0, n_s = 0, rg = 0;
@@ -303,10 +320,10 @@ __global__ void __launch_bounds__(192, 2)
       int nxt = load_entry(win0 + 32 + lane);
       const int n_st = (tok_end - tok_begin + kUmmaKeys - 1) / kUmmaKeys;
       for (int j = 0; j < n_st; ++j) {
-        const int st = i % NST;
-        if (i >= NST) {
+        const int sk = i % NK, sv = i % NV;
+        if (i >= NK) {  // K slot: the PV of stage i - NK has read its K and P
           bool w = true;
-          if (lane == 0) w = mbar_wait(empty0 + 8 * st, ((i / NST) - 1) & 1, limit, flags);
+          if (lane == 0) w = mbar_wait(emptyk0 + 8 * sk, ((i / NK) - 1) & 1, limit, flags);
           ok = __shfl_sync(0xffffffffu, w, 0);
           if (!ok) break;
         }
@@ -327,7 +344,7 @@ __global__ void __launch_bounds__(192, 2)
         }
         const unsigned valid_mask = __ballot_sync(0xffffffffu, y >= 0);
         if (lane == 0) {
-          UmmaStage &h = info[st];
+          UmmaStage &h = info[sk];
           h.row0 = row0;
           h.kvh = kvh;
           h.part = part;
@@ -336,19 +353,33 @@ __global__ void __launch_bounds__(192, 2)
           h.flags = (j == 0 ? kStageFirst : 0) | (j == n_st - 1 ? kStageLast : 0);
           h.rows = ntok * G;
           h.lim_base = lim_base;
-          mbar_arrive_expect_tx(full0 + 8 * st,
-                                (uint32_t)__popc(valid_mask) * U * 128u * NPANELS * 2u);
+          mbar_arrive_expect_tx(fullk0 + 8 * sk, (uint32_t)__popc(valid_mask) * U * 128u * NPANELS);
         }
         __syncwarp();
+        // rows lane*U .. of every panel: [panel][64 rows][128 B] per tensor
         if (y >= 0) {
-          // rows lane*U .. of every panel: [panel][64 rows][128 B] per tensor
-          const uint32_t kdst = ring_u32 + (uint32_t)st * kUmmaStageBytes + (uint32_t)(lane * U) * 128u;
+          const uint32_t kdst = kring_u32 + (uint32_t)sk * kUmmaHalf + (uint32_t)(lane * U) * 128u;
 #pragma unroll
-          for (int pn = 0; pn < NPANELS; ++pn) {
-            tma_load_2d(kdst + pn * kUmmaPanel, &tmap_k, pn * 64, y, full0 + 8 * st);
-            tma_load_2d(kdst + kUmmaHalf + pn * kUmmaPanel, &tmap_v, pn * 64, y, full0 + 8 * st);
-          }
+          for (int pn = 0; pn < NPANELS; ++pn)
+            tma_load_2d(kdst + pn * kUmmaPanel, &tmap_k, pn * 64, y, fullk0 + 8 * sk);
         }
+        ik = i + 1;
+        if (i >= NV) {  // V slot: the PV of stage i - NV has read it
+          bool w = true;
+          if (lane == 0) w = mbar_wait(emptyv0 + 8 * sv, ((i / NV) - 1) & 1, limit, flags);
+          ok = __shfl_sync(0xffffffffu, w, 0);
+          if (!ok) break;
+        }
+        if (lane == 0)
+          mbar_arrive_expect_tx(fullv0 + 8 * sv, (uint32_t)__popc(valid_mask) * U * 128u * NPANELS);
+        __syncwarp();
+        if (y >= 0) {
+          const uint32_t vdst = vring_u32 + (uint32_t)sv * kUmmaHalf + (uint32_t)(lane * U) * 128u;
+#pragma unroll
+          for (int pn = 0; pn < NPANELS; ++pn)
+            tma_load_2d(vdst + pn * kUmmaPanel, &tmap_v, pn * 64, y, fullv0 + 8 * sv);
+        }
+        iv = i + 1;
         if (j == 0) next_raw = grab_issue();
         ++i;
         const int next_rel = ((stage_tok0 + kUmmaKeys) >> p.log2_block_size) - win0;
@@ -362,27 +393,28 @@ __global__ void __launch_bounds__(192, 2)
       item = grab_value(next_raw);
     }
     pdl_launch_dependents();
-    if (ok) {  // no more items
-      const int st = i % NST;
-      if (i >= NST) {
+    if (ok) {  // no more items: a K slot's header says so
+      const int sk = i % NK;
+      if (i >= NK) {
         bool w = true;
-        if (lane == 0) w = mbar_wait(empty0 + 8 * st, ((i / NST) - 1) & 1, limit, flags);
+        if (lane == 0) w = mbar_wait(emptyk0 + 8 * sk, ((i / NK) - 1) & 1, limit, flags);
         ok = __shfl_sync(0xffffffffu, w, 0);
       }
       if (ok && lane == 0) {
-        info[st].flags = kStageEnd;
-        mbar_arrive(full0 + 8 * st);
+        info[sk].flags = kStageEnd;
+        mbar_arrive(fullk0 + 8 * sk);
       }
-      if (ok) ++i;
+      if (ok) ik = ++i;
     }
     if (!ok && lane == 0) {
       report(p.status, kStatusTimeout);
       flags[0] = 1;
     }
     if (lane == 0) {  // every copy of this CTA lands before it retires
-      const int first = i > NST ? i - NST : 0;
-      for (int j = first; j < i; ++j)
-        mbar_wait(full0 + 8 * (j % NST), (j / NST) & 1, kDrainLimitNs, nullptr);
+      for (int j = ik > NK ? ik - NK : 0; j < ik; ++j)
+        mbar_wait(fullk0 + 8 * (j % NK), (j / NK) & 1, kDrainLimitNs, nullptr);
+      for (int j = iv > NV ? iv - NV : 0; j < iv; ++j)
+        mbar_wait(fullv0 + 8 * (j % NV), (j / NV) & 1, kDrainLimitNs, nullptr);
     }
     __syncwarp();
   } else if (warp == 5) {
@@ -390,10 +422,11 @@ __global__ void __launch_bounds__(192, 2)
     if (lane == 0) {
       bool ok = true;
       int items = 0;
-      // S = Q K^T of stage `st` into S buffer b: D / 16 k-steps; a k-step is
-      // 32 bytes inside a 128-byte panel of Q (128 rows) and of K (64 rows)
-      auto issue_s = [&](int st, int b) {
-        const uint32_t kst = ring_u32 + (uint32_t)st * kUmmaStageBytes;
+      // S = Q K^T of the stage in K slot `sk` into S buffer b: D / 16
+      // k-steps; a k-step is 32 bytes inside a 128-byte panel of Q (128 rows)
+      // and of K (64 rows)
+      auto issue_s = [&](int sk, int b) {
+        const uint32_t kst = kring_u32 + (uint32_t)sk * kUmmaHalf;
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
           const uint32_t koff = (uint32_t)(ks & 3) * 32u;
@@ -409,7 +442,7 @@ __global__ void __launch_bounds__(192, 2)
       // work on stage i; within an item only, since a new item's S needs its
       // queries, which the softmax warps store after the item before ends.
       UmmaStage h{};
-      ok = mbar_wait(full0, 0, limit, flags);
+      ok = mbar_wait(fullk0, 0, limit, flags);
       if (ok) h = info[0];
       bool more = ok && !(h.flags & kStageEnd);
       if (more) {
@@ -422,40 +455,43 @@ __global__ void __launch_bounds__(192, 2)
         more = ok;
       }
       for (int i = 0; more; ++i) {
-        const int st = i % NST, st1 = (i + 1) % NST;
-        const uint32_t par1 = ((i + 1) / NST) & 1;
+        const int sk = i % NK, sv = i % NV, sk1 = (i + 1) % NK;
+        const uint32_t par1 = ((i + 1) / NK) & 1;
         // the next stage's S goes first only if its bytes are already here:
         // the PV of this stage never waits for the next stage's copies
         bool s1 = false;
         UmmaStage h1{};
-        if (mbar_test(full0 + 8 * st1, par1)) {
-          h1 = info[st1];
+        if (mbar_test(fullk0 + 8 * sk1, par1)) {
+          h1 = info[sk1];
           if (!(h1.flags & (kStageEnd | kStageFirst))) {
             tc_fence_after();
-            issue_s(st1, (i + 1) & 1);
+            issue_s(sk1, (i + 1) & 1);
             s1 = true;
           }
         }
         ok = mbar_wait(p_full + 8 * (i & 1), (i >> 1) & 1, limit, flags);
         if (!ok) break;
+        ok = mbar_wait(fullv0 + 8 * sv, (i / NV) & 1, limit, flags);  // the stage's V is in
+        if (!ok) break;
         tc_fence_after();
         // O += P V: 4 k-steps of 16 keys; P [128 rows][64 keys] over the K
         // bytes, V MN-major: 64 columns a panel (LBO), 8 keys a 1024-byte
         // group (SBO)
-        const uint32_t kst = ring_u32 + (uint32_t)st * kUmmaStageBytes;
-        const uint32_t vst = kst + kUmmaHalf;
+        const uint32_t kst = kring_u32 + (uint32_t)sk * kUmmaHalf;
+        const uint32_t vst = vring_u32 + (uint32_t)sv * kUmmaHalf;
 #pragma unroll
         for (int kk = 0; kk < kUmmaKeys / 16; ++kk) {
           const uint64_t da = smem_desc(kst + (uint32_t)kk * 32u, 16, 1024);
           const uint64_t db = smem_desc(vst + (uint32_t)kk * 2048u, kUmmaPanel, 1024);
           tc_mma(tmem_o, da, db, kIdescPV, ((h.flags & kStageFirst) && kk == 0) ? 0u : 1u);
         }
-        tc_commit(empty0 + 8 * st);  // the stage's K, P and V are read
+        tc_commit(emptyk0 + 8 * sk);  // the stage's K and P are read
+        tc_commit(emptyv0 + 8 * sv);  // and its V
         if (h.flags & kStageLast) tc_commit(o_done);
         if (!s1) {
-          ok = mbar_wait(full0 + 8 * st1, par1, limit, flags);
+          ok = mbar_wait(fullk0 + 8 * sk1, par1, limit, flags);
           if (!ok) break;
-          h1 = info[st1];
+          h1 = info[sk1];
           if (h1.flags & kStageEnd) break;
           if (h1.flags & kStageFirst) {
             ok = mbar_wait(q_full, items & 1, limit, flags);
@@ -463,7 +499,7 @@ __global__ void __launch_bounds__(192, 2)
             ++items;
           }
           tc_fence_after();
-          issue_s(st1, (i + 1) & 1);
+          issue_s(sk1, (i + 1) & 1);
         }
         h = h1;
       }
@@ -491,14 +527,14 @@ __global__ void __launch_bounds__(192, 2)
       ok = __all_sync(0xffffffffu, ok);
     }
     for (int i = 0; ok; ++i) {
-      const int st = i % NST;
-      const bool w = mbar_wait(full0 + 8 * st, (i / NST) & 1, limit, flags);
+      const int sk = i % NK, sv = i % NV;
+      const bool w = mbar_wait(fullk0 + 8 * sk, (i / NK) & 1, limit, flags);
       ok = __all_sync(0xffffffffu, w);
       if (!ok) break;
-      const UmmaStage h = info[st];
+      const UmmaStage h = info[sk];
       if (h.flags & kStageEnd) break;
-      uint8_t *kst = ring + (size_t)st * kUmmaStageBytes;
-      uint8_t *vst = kst + kUmmaHalf;
+      uint8_t *kst = kring + (size_t)sk * kUmmaHalf;
+      uint8_t *vst = vring + (size_t)sv * kUmmaHalf;
       const int orow_tok = r / G, orow_head = h.kvh * G + r % G;
       if (h.flags & kStageFirst) {
         // this row's query into the swizzled Q tile (zeros past the item's rows)
@@ -563,7 +599,7 @@ __global__ void __launch_bounds__(192, 2)
         // released that stage's slot
         {
           const int ip = i - 1;
-          const bool w4 = mbar_wait(empty0 + 8 * (ip % NST), (ip / NST) & 1, limit, flags);
+          const bool w4 = mbar_wait(emptyv0 + 8 * (ip % NV), (ip / NV) & 1, limit, flags);
           ok = __all_sync(0xffffffffu, w4);
           if (!ok) break;
         }
@@ -603,6 +639,11 @@ __global__ void __launch_bounds__(192, 2)
       // V rows past the range may hold stale or foreign bytes (0 x NaN would
       // reach O): zero them
       if (h.valid < kUmmaKeys) {
+        {  // the stage's V must have landed
+          const bool w5 = mbar_wait(fullv0 + 8 * sv, (i / NV) & 1, limit, flags);
+          ok = __all_sync(0xffffffffu, w5);
+          if (!ok) break;
+        }
         const int n = (kUmmaKeys - h.valid) * (D * (int)sizeof(T) / 16);
         for (int idx = r; idx < n; idx += 128) {
           const int row = h.valid + idx / (D * (int)sizeof(T) / 16);
@@ -686,8 +727,8 @@ __global__ void __launch_bounds__(192, 2)
 }
 
 size_t umma_chunk_smem_bytes() {
-  return 1024 + (size_t)kUmmaStages * kUmmaStageBytes + kUmmaQBytes +
-         kUmmaStages * sizeof(UmmaStage) + (2 * kUmmaStages + 8) * 8 + 32;
+  return (size_t)(kUmmaKSlots + kUmmaVSlots) * kUmmaHalf + kUmmaQBytes +
+         kUmmaKSlots * sizeof(UmmaStage) + (2 * kUmmaKSlots + 2 * kUmmaVSlots + 8) * 8 + 32;
 }
 
 AttnKernelInfo attn_kernel_umma_chunk(int dtype_bf16) {
