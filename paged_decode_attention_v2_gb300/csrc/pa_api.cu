@@ -318,22 +318,28 @@ AttnKernelInfo pick_kernel(int math, int dtype, int head_size, int group) {
   return AttnKernelInfo{nullptr, 0, 0, 0};
 }
 
-// The cache as TMA sees it for the tcgen05 chunk kernel: rows of head_size
-// elements, a box of one 128-byte panel x unit_rows rows (a stage keeps each
-// panel's rows together: [panel][row][128 bytes]).
-pa_status_t encode_cache_map_2d(CUtensorMap *map, const void *base, int dtype, int head_size,
-                                long long rows, int unit_rows) {
+// The cache as TMA sees it for the tcgen05 chunk kernel: (128-byte panel
+// slice, row within an 8-row group, panel, 8-row group), so that one box of
+// (64 elements, 8 rows, every panel, unit_rows / 8 groups) brings all panels
+// of a page's rows and lands as [group][panel][8 rows][128 bytes]: each
+// 8-row group of a panel is one 1024-byte swizzle atom, and the matrix
+// descriptors step 2048 bytes (D 128) from group to group.
+pa_status_t encode_cache_map_umma(CUtensorMap *map, const void *base, int dtype, int head_size,
+                                  long long rows, int unit_rows) {
   PFN_cuTensorMapEncodeTiled_v12000 enc;
   pa_status_t st = get_encoder(&enc);
   if (st != PA_OK) return st;
   const int elt = elt_size(dtype);
+  const int panel = kPanelBytes / elt;
+  const int panels = head_size / panel;
   CUtensorMapDataType dt = dtype == PA_DTYPE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                                   : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-  cuuint64_t gdim[2] = {(cuuint64_t)head_size, (cuuint64_t)rows};
-  cuuint64_t gstride[1] = {(cuuint64_t)head_size * elt};
-  cuuint32_t box[2] = {(cuuint32_t)(kPanelBytes / elt), (cuuint32_t)unit_rows};
-  cuuint32_t estride[2] = {1, 1};
-  CUresult r = enc(map, dt, 2, const_cast<void *>(base), gdim, gstride, box, estride,
+  cuuint64_t gdim[4] = {(cuuint64_t)panel, 8, (cuuint64_t)panels, (cuuint64_t)(rows / 8)};
+  cuuint64_t gstride[3] = {(cuuint64_t)head_size * elt, (cuuint64_t)kPanelBytes,
+                           (cuuint64_t)head_size * elt * 8};
+  cuuint32_t box[4] = {(cuuint32_t)panel, 8, (cuuint32_t)panels, (cuuint32_t)(unit_rows / 8)};
+  cuuint32_t estride[4] = {1, 1, 1, 1};
+  CUresult r = enc(map, dt, 4, const_cast<void *>(base), gdim, gstride, box, estride,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
@@ -508,7 +514,7 @@ pa_status_t launch(const Call &c, bool v2, const pa_options_t &opt) {
   const int unit_rows = c.block_size < k.stage_tokens ? c.block_size : k.stage_tokens;
   const long long rows = (long long)c.num_blocks * c.num_kv_heads * c.block_size;
   CUtensorMap tmap_k, tmap_v;
-  auto encode = k.umma ? encode_cache_map_2d : encode_cache_map;
+  auto encode = k.umma ? encode_cache_map_umma : encode_cache_map;
   st = encode(&tmap_k, c.key_cache, c.dtype, c.head_size, rows, unit_rows);
   if (st != PA_OK) return st;
   st = encode(&tmap_v, c.value_cache, c.dtype, c.head_size, rows, unit_rows);

@@ -32,8 +32,11 @@ constexpr int kUmmaTmemCols = 256;    // S at columns 0 and 64 (two buffers), O 
 // K of stage i + 1 then loads while stage i - 1's PV runs.
 constexpr int kUmmaKSlots = 3;
 constexpr int kUmmaVSlots = 2;
-constexpr int kUmmaPanel = kUmmaKeys * 128;             // one 128-byte panel of a stage's rows
-constexpr int kUmmaHalf = (kUmmaD * 2 / 128) * kUmmaPanel;  // K (or V) bytes of a stage
+// A K (or V) slot holds 64 keys as [8-key group][panel][8 keys][128 B]: each
+// 8-row piece of a panel is one 1024-byte swizzle atom, a group is kUmmaGroup
+// bytes (every panel), and a page's rows arrive in one 4-D copy.
+constexpr int kUmmaGroup = (kUmmaD * 2 / 128) * 1024;
+constexpr int kUmmaHalf = (kUmmaKeys / 8) * kUmmaGroup;  // K (or V) bytes of a stage
 constexpr int kUmmaQPanel = kUmmaRows * 128;
 constexpr int kUmmaQBytes = (kUmmaD * 2 / 128) * kUmmaQPanel;
 constexpr float kLazyMargin = 8.f;    // log2 units
@@ -356,12 +359,10 @@ __global__ void __launch_bounds__(192, 2)
           mbar_arrive_expect_tx(fullk0 + 8 * sk, (uint32_t)__popc(valid_mask) * U * 128u * NPANELS);
         }
         __syncwarp();
-        // rows lane*U .. of every panel: [panel][64 rows][128 B] per tensor
+        // rows lane*U .. : groups lane*U/8 .. of the slot, every panel, one copy
         if (y >= 0) {
-          const uint32_t kdst = kring_u32 + (uint32_t)sk * kUmmaHalf + (uint32_t)(lane * U) * 128u;
-#pragma unroll
-          for (int pn = 0; pn < NPANELS; ++pn)
-            tma_load_2d(kdst + pn * kUmmaPanel, &tmap_k, pn * 64, y, fullk0 + 8 * sk);
+          const uint32_t kdst = kring_u32 + (uint32_t)sk * kUmmaHalf + (uint32_t)(lane * U / 8) * kUmmaGroup;
+          tma_load_4d(kdst, &tmap_k, 0, 0, 0, y >> 3, fullk0 + 8 * sk);
         }
         ik = i + 1;
         if (i >= NV) {  // V slot: the PV of stage i - NV has read it
@@ -374,10 +375,8 @@ __global__ void __launch_bounds__(192, 2)
           mbar_arrive_expect_tx(fullv0 + 8 * sv, (uint32_t)__popc(valid_mask) * U * 128u * NPANELS);
         __syncwarp();
         if (y >= 0) {
-          const uint32_t vdst = vring_u32 + (uint32_t)sv * kUmmaHalf + (uint32_t)(lane * U) * 128u;
-#pragma unroll
-          for (int pn = 0; pn < NPANELS; ++pn)
-            tma_load_2d(vdst + pn * kUmmaPanel, &tmap_v, pn * 64, y, fullv0 + 8 * sv);
+          const uint32_t vdst = vring_u32 + (uint32_t)sv * kUmmaHalf + (uint32_t)(lane * U / 8) * kUmmaGroup;
+          tma_load_4d(vdst, &tmap_v, 0, 0, 0, y >> 3, fullv0 + 8 * sv);
         }
         iv = i + 1;
         if (j == 0) next_raw = grab_issue();
@@ -423,15 +422,16 @@ __global__ void __launch_bounds__(192, 2)
       bool ok = true;
       int items = 0;
       // S = Q K^T of the stage in K slot `sk` into S buffer b: D / 16
-      // k-steps; a k-step is 32 bytes inside a 128-byte panel of Q (128 rows)
-      // and of K (64 rows)
+      // k-steps; a k-step is 32 bytes inside a 128-byte panel of Q (128 rows,
+      // 8-row atoms 1024 bytes apart, panels 16 KB apart) and of K (8-key
+      // groups kUmmaGroup bytes apart, panels 1024 bytes apart)
       auto issue_s = [&](int sk, int b) {
         const uint32_t kst = kring_u32 + (uint32_t)sk * kUmmaHalf;
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
           const uint32_t koff = (uint32_t)(ks & 3) * 32u;
           const uint64_t da = smem_desc(q_u32 + (uint32_t)(ks >> 2) * kUmmaQPanel + koff, 16, 1024);
-          const uint64_t db = smem_desc(kst + (uint32_t)(ks >> 2) * kUmmaPanel + koff, 16, 1024);
+          const uint64_t db = smem_desc(kst + (uint32_t)(ks >> 2) * 1024u + koff, 16, kUmmaGroup);
           tc_mma(tmem_s + 64u * (uint32_t)b, da, db, kIdescS, ks > 0 ? 1u : 0u);
         }
         tc_commit(s_full + 8u * (uint32_t)b);
@@ -475,14 +475,14 @@ __global__ void __launch_bounds__(192, 2)
         if (!ok) break;
         tc_fence_after();
         // O += P V: 4 k-steps of 16 keys; P [128 rows][64 keys] over the K
-        // bytes, V MN-major: 64 columns a panel (LBO), 8 keys a 1024-byte
-        // group (SBO)
+        // bytes (8 rows a 1024-byte atom), V MN-major: 64 columns a panel
+        // 1024 bytes apart (LBO), 8 keys a group kUmmaGroup bytes apart (SBO)
         const uint32_t kst = kring_u32 + (uint32_t)sk * kUmmaHalf;
         const uint32_t vst = vring_u32 + (uint32_t)sv * kUmmaHalf;
 #pragma unroll
         for (int kk = 0; kk < kUmmaKeys / 16; ++kk) {
           const uint64_t da = smem_desc(kst + (uint32_t)kk * 32u, 16, 1024);
-          const uint64_t db = smem_desc(vst + (uint32_t)kk * 2048u, kUmmaPanel, 1024);
+          const uint64_t db = smem_desc(vst + (uint32_t)kk * 2u * kUmmaGroup, 1024, kUmmaGroup);
           tc_mma(tmem_o, da, db, kIdescPV, ((h.flags & kStageFirst) && kk == 0) ? 0u : 1u);
         }
         tc_commit(emptyk0 + 8 * sk);  // the stage's K and P are read
@@ -648,7 +648,8 @@ __global__ void __launch_bounds__(192, 2)
         for (int idx = r; idx < n; idx += 128) {
           const int row = h.valid + idx / (D * (int)sizeof(T) / 16);
           const int c = idx % (D * (int)sizeof(T) / 16);
-          *reinterpret_cast<uint4 *>(vst + (c >> 3) * kUmmaPanel + row * 128 + (((c & 7) ^ (row & 7)) << 4)) =
+          *reinterpret_cast<uint4 *>(vst + (row >> 3) * kUmmaGroup + (c >> 3) * 1024 + (row & 7) * 128 +
+                                     (((c & 7) ^ (row & 7)) << 4)) =
               make_uint4(0u, 0u, 0u, 0u);
         }
       }
