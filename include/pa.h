@@ -346,10 +346,10 @@ int pa_choose_v2(int num_seqs, int num_kv_heads, int max_seq_len,
  * rows per KV head, pa_choose_v2's answer; otherwise V1 when the batch has
  * at least 8 work items per SM (4 on the tcgen05 kernel), counting an item
  * per (sequence, KV head) and row group as the chunk kernels cut them (128
- * rows on the tcgen05 kernel: at least 128 rows per KV head at head_size
- * 128; 64 on the row-owning kernel: more than 32 rows per KV head,
- * head_size 64 or 128, a group dividing 64; else 16), V2 below (measured on
- * GB300).  Pure host arithmetic on its arguments. */
+ * rows on the tcgen05 kernel: more than 16 rows per KV head at head_size
+ * 128; 64 on the row-owning kernel: more than 32 rows per KV head at
+ * head_size 64, a group dividing 64; else 16), V2 below (measured on GB300).
+ * Pure host arithmetic on its arguments. */
 int pa_choose_v2_chunks(int num_seqs, int num_heads, int num_kv_heads, int head_size,
                         int max_chunk, int max_seq_len, int partition_size, int sm_count);
 

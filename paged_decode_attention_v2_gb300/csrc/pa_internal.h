@@ -92,10 +92,14 @@ struct AttnKernelInfo {
   int umma;           // 1: the tcgen05 query-chunk kernel (its own layout and launch)
 };
 
-// Query chunks on tcgen05: D 128, 16-bit, at least one full 128-row item per
-// KV head.
+// Query chunks on tcgen05: D 128, 16-bit, more than 16 rows per KV head.  A
+// 128-row item costs about the same however many of its rows are live, and
+// the two-n-tile kernel needs one 16-row item per 16 rows: measured on GB300
+// (the 256-sequence cache, 8 heads a group) the tcgen05 kernel is ahead from
+// 32 rows (0.260 against 0.293 ms at 4 tokens, 0.258 against 0.426 at 8) and
+// behind at 16 (0.258 against 0.193 ms).
 inline bool umma_chunk_ok(int head_size, int group, long long max_rows) {
-  return head_size == 128 && group >= 1 && 128 % group == 0 && max_rows >= 128;
+  return head_size == 128 && group >= 1 && 128 % group == 0 && max_rows > 16;
 }
 AttnKernelInfo attn_kernel_umma_chunk(int dtype_bf16);
 size_t umma_chunk_smem_bytes();

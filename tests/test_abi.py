@@ -97,7 +97,7 @@ def test_choose_v2_matches_the_measured_crossover(lib, cell):
 CHUNK_SHAPES = {"c4": (256, 32, 4, 128, 3584), "c2": (8, 32, 4, 128, 8192),
                 "c3": (1, 32, 4, 128, 100000)}
 CHOOSE_V2_CHUNKS_MEASURED = {
-    ("c4", 2): 1, ("c4", 4): 0, ("c4", 8): 1, ("c4", 16): 0, ("c4", 32): 0, ("c4", 64): 0,
+    ("c4", 2): 1, ("c4", 4): 0, ("c4", 8): 0, ("c4", 16): 0, ("c4", 32): 0, ("c4", 64): 0,
     ("c2", 4): 1, ("c2", 16): 1, ("c2", 64): 1, ("c3", 16): 1, ("c3", 64): 1,
 }
 

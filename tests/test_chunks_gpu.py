@@ -3,8 +3,8 @@ oracle's query_chunks, element by element: chunks of the last n tokens of
 each sequence, causal among themselves, over V1 / V2 / auto, every tensor
 dtype, head size and a spread of group sizes (which set how many chunk
 tokens an item holds: 16 / G on the two-n-tile kernel, 64 / G on the
-row-owning one, 128 / G on the tcgen05 one, which takes chunks of at least
-128 rows per KV head at D 128)."""
+row-owning one (D 64), 128 / G on the tcgen05 one, which takes chunks of
+more than 16 rows per KV head at D 128)."""
 import pytest
 import torch
 
@@ -34,7 +34,7 @@ CASES = [  # dtype, D, G, Hkv, bs, P, lens, qlens
     (torch.bfloat16, 256, 2, 2, 32, 512, [3000, 1200], [12, 8]),
     (torch.float16, 128, 1, 8, 16, 512, [2500, 600, 17], [20, 3, 17]),  # 16 tokens an item
     (torch.bfloat16, 64, 16, 1, 64, 256, [5000, 260], [2, 1]),           # one token an item
-    # tcgen05 kernel (>= 128 rows per KV head at D 128): f16, pages of 32, 8 and 64 tokens,
+    # tcgen05 kernel (> 16 rows per KV head at D 128): f16, pages of 32, 8 and 64 tokens,
     # a chunk that is its whole sequence, ragged row groups
     (torch.float16, 128, 4, 2, 32, 512, [1000, 2100, 70], [40, 64, 70]),
     (torch.bfloat16, 128, 16, 1, 8, 256, [600, 1300], [9, 13]),
