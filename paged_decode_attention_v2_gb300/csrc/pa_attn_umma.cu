@@ -556,10 +556,42 @@ __global__ void __launch_bounds__(192, 2)
         __syncwarp();
         if (lane == 0) mbar_arrive(q_full);
       }
+      // Every warp waits for the stage's S: S(i) is issued only after the P of
+      // stage i - 2 was taken, so no warp's P-ready arrival can land in the
+      // phase of another stage.
       {
         const bool w2 = mbar_wait(s_full + 8 * (i & 1), (i >> 1) & 1, limit, flags);
         ok = __all_sync(0xffffffffu, w2);
         if (!ok) break;
+      }
+      // A warp whose 32 rows are all past the item's rows skips its scores,
+      // softmax and P: its rows of P hold stale bytes, which reach only
+      // those rows of O (each row of O depends on its own row of P alone),
+      // and they are never written out.
+      const bool warp_live = 32 * warp < h.rows;
+      if (!warp_live) {
+        // only its share of zeroing the V rows past the range (below), and
+        // the P-ready arrival
+        if (h.valid < kUmmaKeys) {
+          {  // the stage's V must have landed
+            const bool w5 = mbar_wait(fullv0 + 8 * sv, (i / NV) & 1, limit, flags);
+            ok = __all_sync(0xffffffffu, w5);
+            if (!ok) break;
+          }
+          const int n = (kUmmaKeys - h.valid) * (D * (int)sizeof(T) / 16);
+          for (int idx = r; idx < n; idx += 128) {
+            const int row = h.valid + idx / (D * (int)sizeof(T) / 16);
+            const int c = idx % (D * (int)sizeof(T) / 16);
+            *reinterpret_cast<uint4 *>(vst + (row >> 3) * kUmmaGroup + (c >> 3) * 1024 + (row & 7) * 128 +
+                                       (((c & 7) ^ (row & 7)) << 4)) =
+                make_uint4(0u, 0u, 0u, 0u);
+          }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(p_full + 8 * (i & 1));
+        if (h.flags & kStageLast) ++items;  // this warp has no rows to write
+        continue;
       }
       tc_fence_after();
       uint32_t sa[32], sb[32];
@@ -572,17 +604,17 @@ __global__ void __launch_bounds__(192, 2)
       // (key index kvis and up) get -inf, a step every row of the warp skips
       // when all of them see the whole stage
       float x[64];
-#pragma unroll
+  #pragma unroll
       for (int k = 0; k < 64; ++k) x[k] = __uint_as_float(k < 32 ? sa[k] : sb[k - 32]) * p.scale_log2;
       const int kvis = min(h.valid, lim - h.tok0);
       if (!__all_sync(0xffffffffu, kvis >= kUmmaKeys)) {
-#pragma unroll
+  #pragma unroll
         for (int k = 0; k < 64; ++k)
           if (k >= kvis) x[k] = -CUDART_INF_F;
       }
       // the row maximum: 8 chains of three-input maxima over 8 keys each
       float m8[8];
-#pragma unroll
+  #pragma unroll
       for (int j = 0; j < 8; ++j) {
         const float *v = x + 8 * j;
         m8[j] = fmax3(fmax3(v[0], v[1], v[2]), fmax3(v[3], v[4], v[5]), fmaxf(v[6], v[7]));
@@ -604,12 +636,12 @@ __global__ void __launch_bounds__(192, 2)
           if (!ok) break;
         }
         tc_fence_after();
-#pragma unroll
+  #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t o[32];
           tmem_ld32(tmem_o + lane_off + 32 * c, o);
           tmem_ld_wait(o);
-#pragma unroll
+  #pragma unroll
           for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
           tmem_st32(tmem_o + lane_off + 32 * c, o);
         }
@@ -623,10 +655,10 @@ __global__ void __launch_bounds__(192, 2)
       // and unbiased.  Row r of P [128][64 keys] over the stage's K bytes,
       // 128-byte swizzle.
       float l4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
+  #pragma unroll
       for (int c = 0; c < 8; ++c) {
         uint32_t w4[4];
-#pragma unroll
+  #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const float p0 = ex2(x[8 * c + 2 * e] - mb), p1 = ex2(x[8 * c + 2 * e + 1] - mb);
           l4[e] += p0 + p1;
