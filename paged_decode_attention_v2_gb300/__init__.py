@@ -279,7 +279,7 @@ def pa_forward(out, query, key_cache, value_cache, block_tables, seq_lens, scale
 def pa_chunks_forward(out, query, key_cache, value_cache, block_tables, seq_lens, q_start,
                       scale, partition_size, workspace, max_seq_len=None, max_chunk=None,
                       stream=None, variant=PA_VARIANT_AUTO, num_stages=0, ctas_per_sm=0,
-                      phase1_event=None, debug_flags=0) -> None:
+                      phase1_event=None, debug_flags=0, wait_limit_ns=0) -> None:
     """Multi-token queries over the paged cache (see include/pa.h): query and
     out [num_rows, H, D]; the chunk of sequence s is rows q_start[s] ..
     q_start[s+1]-1 (int32 on the device), its last tokens.  max_chunk bounds
@@ -294,7 +294,7 @@ def pa_chunks_forward(out, query, key_cache, value_cache, block_tables, seq_lens
     if max_seq_len is None:
         max_seq_len = block_tables.shape[1] * bs
     mc = int(max_chunk) if max_chunk is not None else int(max_seq_len)
-    opts = pa_options_t(variant, PA_MATH_AUTO, num_stages, debug_flags, 0,
+    opts = pa_options_t(variant, PA_MATH_AUTO, num_stages, debug_flags, wait_limit_ns,
                         _event_handle(phase1_event), ctas_per_sm, 0)
     _check(load_library().pa_chunks_forward(
         _ptr(out), _ptr(query), _ptr(key_cache), _ptr(value_cache), _ptr(block_tables),
