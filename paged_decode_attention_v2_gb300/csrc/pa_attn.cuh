@@ -1400,13 +1400,15 @@ AttnKernelInfo select_tensor(int D, int group) {
   return AttnKernelInfo{nullptr, 0, 0, 0};
 }
 
-// Query chunks.  Chunks of more than 32 (token, head) rows per KV head run on
-// row-owning warps (64 keys a stage, items of 64 rows, four consumer warps)
-// for D 64 and 128 when the group divides 64; measured on GB300, that is
-// 1.3x the two-n-tile path at 16 and 64 tokens of 8 heads, while 32-row items
-// (two consumer warps, one per SM sub-partition) were slower than it at
-// 4 tokens.  Everything else runs on the two-n-tile tensor path, 16 rows an
-// item.
+// Query chunks on mma.sync.  (At D 128 the host sends chunks of more than 16
+// rows per KV head to the tcgen05 kernel, unless told not to; these kernels
+// then serve D 64 and 256, up to 16 rows at D 128, and that comparison.)
+// Chunks of more than 32 (token, head) rows per KV head run on row-owning
+// warps (64 keys a stage, items of 64 rows, four consumer warps) for D 64 and
+// 128 when the group divides 64; measured on GB300, that is 1.3x the
+// two-n-tile path at 16 and 64 tokens of 8 heads, while 32-row items (two
+// consumer warps, one per SM sub-partition) were slower than it at 4 tokens.
+// Everything else runs on the two-n-tile tensor path, 16 rows an item.
 template <typename T>
 AttnKernelInfo select_chunk(int D, int group, int max_rows) {
   if ((D == 64 || D == 128) && 64 % group == 0 && max_rows > 32) {
