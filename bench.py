@@ -40,6 +40,7 @@ import json
 import math
 import os
 import platform
+import re
 import statistics
 import subprocess
 import sys
@@ -188,13 +189,23 @@ def measured_hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_source_digest() -> str:
+def _code_only(text: str) -> str:
+    """C++ source without its comments and with whitespace collapsed: what the
+    compiler sees, up to formatting."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
+def kernel_source_digest(csrc: str = None) -> str:
+    """Digest of the kernel sources' code (comments and formatting ignored), so
+    that a traffic record stays attached to the code it was measured on."""
     h = hashlib.sha256()
-    csrc = os.path.join(ROOT, "paged_decode_attention_v2_gb300", "csrc")
+    csrc = csrc or os.path.join(ROOT, "paged_decode_attention_v2_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
         if name.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode() + f.read())
+            with open(os.path.join(csrc, name), encoding="utf-8") as f:
+                h.update(name.encode() + _code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 
