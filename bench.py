@@ -357,10 +357,11 @@ class ChunkRunner:
     """The same cache as a Runner, queried with chunks of `tokens` tokens per
     sequence (pa_chunks_forward), in `layers` copies."""
 
-    def __init__(self, case, device, tokens, layers=1):
+    def __init__(self, case, device, tokens, layers=1, share_kv=0):
         import paged_decode_attention_v2_gb300 as pa
         self.pa = pa
         self.case = case
+        self.share_kv = share_kv
         q, qs = workloads.chunk_queries(case, tokens)
         q = q.to(device)
         self.q_start = qs.to(device)
@@ -391,7 +392,8 @@ class ChunkRunner:
         self.pa.pa_chunks_forward(out, q, kc, vc, self.bt, self.sl,
                                   self.q_start, self.case.scale, self.case.partition_size,
                                   self.ws, max_seq_len=self.case.max_seq_len,
-                                  max_chunk=self.tokens, phase1_event=phase1_event)
+                                  max_chunk=self.tokens, phase1_event=phase1_event,
+                                  share_kv=self.share_kv)
 
     def check_status(self):
         st = self.pa.pa_read_device_status(self.ws)
@@ -777,6 +779,14 @@ def run_ours(args):
         flops = 4.0 * case.num_heads * LONG_CHUNK_TOKENS * vis * case.head_size
         ce["attention_tflops"] = round(flops / (ce["ms_per_step"] / 1e3) / 1e12, 1)
         ce["rows"] = rows
+        # the same step with the row groups of each (sequence, KV head) in a
+        # thread-block cluster sharing every K/V stage (share_kv): K/V cross
+        # HBM once instead of once per row group
+        cr.share_kv = 1
+        se = measure(args.workload, case, cr, flush, peak, 20, 20)
+        ce["shared_kv"] = {"ms_per_step": se["ms_per_step"],
+                           "attention_tflops": round(flops / (se["ms_per_step"] / 1e3) / 1e12, 1),
+                           "isolated_ms_per_step": se["isolated"]["ms_per_step"]}
         line["long_chunks"] = ce
         del cr
         torch.cuda.empty_cache()

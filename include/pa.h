@@ -88,6 +88,16 @@ typedef struct {
                              (capped at 16) get the cross-partition combine
                              inside the Phase 1 kernel; 0 (the default) or
                              negative = never: the Phase 2 kernel does it */
+  int32_t share_kv;       /* query chunks on the tcgen05 kernel (head_size
+                             128, more than 16 rows per KV head) with 256 or
+                             more rows per KV head: 1 = the CTAs of the row
+                             groups of the same keys form a thread-block
+                             cluster (of 2 or 4) and share every K/V stage
+                             through multicast copies, so that K/V cross HBM
+                             once instead of once per row group; slower on
+                             GB300 when HBM is not the limit (measured
+                             2.5-10 %); 0 (the default) = each CTA loads its
+                             own */
 } pa_options_t;
 
 /* Debug: every consumer warp waits on a barrier that nothing ever releases,
@@ -100,6 +110,7 @@ typedef struct {
  * rows per KV head at head_size 128 then run on the mma.sync row-owning
  * kernel), for comparisons of the two. */
 #define PA_DEBUG_NO_TCGEN05 2
+
 
 /* Bytes of workspace that pa_v2_forward needs (V1 needs only the 256-byte
  * status block).  The partials are the three per-partition arrays that the

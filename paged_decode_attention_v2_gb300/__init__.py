@@ -57,7 +57,8 @@ class pa_options_t(ctypes.Structure):
     _fields_ = [("variant", ctypes.c_int32), ("math", ctypes.c_int32),
                 ("num_stages", ctypes.c_int32), ("debug_flags", ctypes.c_int32),
                 ("wait_limit_ns", ctypes.c_uint64), ("phase1_event", ctypes.c_void_p),
-                ("ctas_per_sm", ctypes.c_int32), ("fuse_partitions", ctypes.c_int32)]
+                ("ctas_per_sm", ctypes.c_int32), ("fuse_partitions", ctypes.c_int32),
+                ("share_kv", ctypes.c_int32)]
 
 
 _lib = None
@@ -279,7 +280,8 @@ def pa_forward(out, query, key_cache, value_cache, block_tables, seq_lens, scale
 def pa_chunks_forward(out, query, key_cache, value_cache, block_tables, seq_lens, q_start,
                       scale, partition_size, workspace, max_seq_len=None, max_chunk=None,
                       stream=None, variant=PA_VARIANT_AUTO, num_stages=0, ctas_per_sm=0,
-                      phase1_event=None, debug_flags=0, wait_limit_ns=0) -> None:
+                      phase1_event=None, debug_flags=0, wait_limit_ns=0,
+                      share_kv=0) -> None:
     """Multi-token queries over the paged cache (see include/pa.h): query and
     out [num_rows, H, D]; the chunk of sequence s is rows q_start[s] ..
     q_start[s+1]-1 (int32 on the device), its last tokens.  max_chunk bounds
@@ -295,7 +297,7 @@ def pa_chunks_forward(out, query, key_cache, value_cache, block_tables, seq_lens
         max_seq_len = block_tables.shape[1] * bs
     mc = int(max_chunk) if max_chunk is not None else int(max_seq_len)
     opts = pa_options_t(variant, PA_MATH_AUTO, num_stages, debug_flags, wait_limit_ns,
-                        _event_handle(phase1_event), ctas_per_sm, 0)
+                        _event_handle(phase1_event), ctas_per_sm, 0, share_kv)
     _check(load_library().pa_chunks_forward(
         _ptr(out), _ptr(query), _ptr(key_cache), _ptr(value_cache), _ptr(block_tables),
         _ptr(seq_lens), _ptr(q_start), B, R, mc, H, hkv, D, nb, bs, block_tables.shape[1],

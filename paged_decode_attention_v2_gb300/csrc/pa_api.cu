@@ -467,8 +467,18 @@ pa_status_t launch(const Call &c, bool v2, const pa_options_t &opt) {
   if (chunk && math != kMathTensor) return PA_ERR_UNSUPPORTED;
   const bool umma = chunk && !(opt.debug_flags & PA_DEBUG_NO_TCGEN05) &&
                     umma_chunk_ok(c.head_size, group, (long long)c.max_chunk * group);
+  // tcgen05 chunks of several 128-row groups per KV head, when asked
+  // (share_kv): a cluster of 2 or 4 CTAs takes them together, sharing each
+  // stage's K/V by multicast.  Off by default: measured on GB300 (the
+  // 256-sequence cache, V1) it reads K/V from HBM once instead of 1.66 times
+  // but takes 10 % longer at 4 CTAs (64-token chunks) and 2.5 % at 2.
+  int cl = 1;
+  if (umma && opt.share_kv > 0) {
+    const long long rg = ((long long)c.max_chunk * group + 127) / 128;
+    cl = rg >= 4 ? 4 : rg >= 2 ? 2 : 1;
+  }
   const AttnKernelInfo k =
-      umma    ? attn_kernel_umma_chunk(c.dtype == PA_DTYPE_BF16 ? 1 : 0)
+      umma    ? attn_kernel_umma_chunk(c.dtype == PA_DTYPE_BF16 ? 1 : 0, cl > 1)
       : chunk ? (c.dtype == PA_DTYPE_BF16
                      ? attn_kernel_chunk_bf16(c.head_size, group, c.max_chunk * group)
                      : attn_kernel_chunk_f16(c.head_size, group, c.max_chunk * group))
@@ -628,11 +638,13 @@ pa_status_t launch(const Call &c, bool v2, const pa_options_t &opt) {
   const long long range_parts =
       v2 ? (long long)(c.part_end < p.max_parts ? c.part_end : p.max_parts) - c.part_begin
          : p.max_parts;
-  const long long max_items =
-      (long long)c.num_seqs * c.num_kv_heads * (range_parts > 0 ? range_parts : 0) *
-      (chunk ? (c.max_chunk + p.chunk_tokens - 1) / p.chunk_tokens : 1);
+  const long long groups = chunk ? (c.max_chunk + p.chunk_tokens - 1) / p.chunk_tokens : 1;
+  p.cluster = cl;
+  const long long max_items = (long long)c.num_seqs * c.num_kv_heads *
+                              (range_parts > 0 ? range_parts : 0) * ((groups + cl - 1) / cl) * cl;
   long long grid = (long long)per_sm * dev->sm_count;
   if (grid > max_items) grid = max_items;
+  grid = grid / cl * cl;  // whole clusters
   if (phase1 && grid > 0) {
     cudaLaunchConfig_t cfg;
     memset(&cfg, 0, sizeof cfg);
@@ -643,11 +655,18 @@ pa_status_t launch(const Call &c, bool v2, const pa_options_t &opt) {
     // Programmatic dependent launch: the kernel's launch and shared-memory
     // set-up overlap the tail of the previous kernel in the stream; the
     // kernel waits for that kernel before its first global access.
-    cudaLaunchAttribute pattr[1];
+    cudaLaunchAttribute pattr[2];
     pattr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     pattr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = pattr;
     cfg.numAttrs = 1;
+    if (cl > 1) {
+      pattr[1].id = cudaLaunchAttributeClusterDimension;
+      pattr[1].val.clusterDim.x = (unsigned)cl;
+      pattr[1].val.clusterDim.y = 1;
+      pattr[1].val.clusterDim.z = 1;
+      cfg.numAttrs = 2;
+    }
     void *args[3] = {&p, &tmap_k, &tmap_v};
     cudaError_t e = cudaLaunchKernelExC(&cfg, k.fn, args);
     if (e != cudaSuccess) return fail_cuda("launch attention kernel", e);

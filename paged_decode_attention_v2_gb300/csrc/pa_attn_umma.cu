@@ -40,6 +40,7 @@ constexpr int kUmmaHalf = (kUmmaKeys / 8) * kUmmaGroup;  // K (or V) bytes of a 
 constexpr int kUmmaQPanel = kUmmaRows * 128;
 constexpr int kUmmaQBytes = (kUmmaD * 2 / 128) * kUmmaQPanel;
 constexpr float kLazyMargin = 8.f;    // log2 units
+constexpr int kMailSlots = 8;         // cluster: items the leader may run ahead of the others
 
 struct UmmaStage {
   int row0, kvh, part;  // the item: first query row, KV head, partition
@@ -98,6 +99,72 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
   asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
                : "memory");
 }
+// ---- thread-block clusters: the CTAs of a cluster take the row groups of
+// the same keys, each issuing a share of every stage's copies into all of them
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// the same shared-memory offset in the CTA of the given rank
+__device__ __forceinline__ uint32_t cluster_addr(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+// every thread of every CTA of the cluster
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
+__device__ __forceinline__ void st_cluster(uint32_t addr, int v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+// one arrival, with release at cluster scope, on an mbarrier of another CTA
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(addr) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// a bounded wait that also acquires what other CTAs of the cluster released
+__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, uint64_t limit_ns,
+                                                  const volatile int *abort) {
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    if (mbar_try_cluster(bar, parity)) return true;
+    if (abort && *abort) return false;
+    if (globaltimer_ns() - t0 > limit_ns) return false;
+  }
+}
+// a 4-D copy landing at the same offset in every CTA of `mask`, each CTA's
+// mbarrier (same offset) counting the bytes it receives
+__device__ __forceinline__ void tma_load_4d_multicast(uint32_t dst, const CUtensorMap *map, int x,
+                                                      int y, int z, int w, uint32_t bar,
+                                                      uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".multicast::cluster [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(bar), "h"(mask)
+      : "memory");
+}
+// one arrival on the mbarrier at this offset in every CTA of `mask` once
+// this thread's earlier tcgen05 operations have completed
+__device__ __forceinline__ void tc_commit_multicast(uint32_t bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(bar),
+      "h"(mask)
+      : "memory");
+}
+
 // max(a, b, c) in one instruction
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float r;
@@ -137,8 +204,9 @@ __host__ __device__ constexpr uint32_t instr_desc(int m, int n, bool b_mn_major)
 
 }  // namespace
 
-template <typename T>
-// two CTAs an SM: at most 168 registers a thread
+// CLUSTERED: launched in thread-block clusters of p.cluster CTAs (else the
+// cluster code compiles away).  Two CTAs an SM: at most 168 registers a thread.
+template <typename T, bool CLUSTERED>
 __global__ void __launch_bounds__(192, 2)
     pa_umma_chunk_kernel(const __grid_constant__ AttnParams p,
                          const __grid_constant__ CUtensorMap tmap_k,
@@ -155,8 +223,19 @@ __global__ void __launch_bounds__(192, 2)
   // relies on the dynamic shared memory starting 1024-byte aligned (it
   // starts right after the 1 KB the system reserves) and checks it.
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  if (smem_u32(smem_raw) & 1023u) {
+  const bool misaligned = (smem_u32(smem_raw) & 1023u) != 0;
+  // CL CTAs a cluster (p.cluster, 1 = none): rank r takes row group
+  // g * CL + r of each cluster item g, the leader (rank 0) takes the items
+  // from the work counter and hands them on
+  const int CL = CLUSTERED && p.cluster > 1 ? p.cluster : 1;
+  const uint32_t rank = CL > 1 ? cluster_rank() : 0u;
+  const uint16_t all_ctas = (uint16_t)((1u << CL) - 1u);
+  if (misaligned) {
     if (threadIdx.x == 0) report(p.status, kStatusBadInput);
+    if (CL > 1) {  // every CTA of the cluster meets both cluster barriers
+      cluster_sync();
+      cluster_sync();
+    }
     return;
   }
   uint8_t *kring = smem_raw;                             // NK x K: [panel][64 keys][128 B]
@@ -169,25 +248,29 @@ __global__ void __launch_bounds__(192, 2)
   // softmax may run one stage ahead of the MMA thread's wait for its P (the
   // next S is issued before this PV), and one barrier for every stage would
   // then complete twice before that wait and never show the awaited phase.
-  constexpr int NBARS = 2 * NK + 2 * NV + 8;
+  // then mail[kMailSlots]: the leader's hand-over of each next item
+  constexpr int NBARS = 2 * NK + 2 * NV + 8 + kMailSlots;
   volatile int *flags = reinterpret_cast<volatile int *>(bars + NBARS);
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + NBARS) + 4;
+  volatile int *mailbox = reinterpret_cast<volatile int *>(bars + NBARS) + 8;  // kMailSlots items
   const uint32_t kring_u32 = smem_u32(kring), vring_u32 = smem_u32(vring), q_u32 = smem_u32(qbuf);
   const uint32_t fullk0 = smem_u32(bars), emptyk0 = fullk0 + 8 * NK;
   const uint32_t fullv0 = emptyk0 + 8 * NK, emptyv0 = fullv0 + 8 * NV;
   const uint32_t q_full = emptyv0 + 8 * NV, s_full = q_full + 8, p_full = s_full + 16,
-                 o_done = p_full + 16, drain = o_done + 8, never = drain + 8;
+                 o_done = p_full + 16, drain = o_done + 8, never = drain + 8, mail0 = never + 8;
   const uint64_t limit = p.wait_limit_ns;
 
   if (threadIdx.x == 0) {
+    // a slot is free once the PV of every CTA of the cluster has read it
     for (int i = 0; i < NK; ++i) {
       mbar_init(fullk0 + 8 * i, 1);
-      mbar_init(emptyk0 + 8 * i, 1);
+      mbar_init(emptyk0 + 8 * i, CL);
     }
     for (int i = 0; i < NV; ++i) {
       mbar_init(fullv0 + 8 * i, 1);
-      mbar_init(emptyv0 + 8 * i, 1);
+      mbar_init(emptyv0 + 8 * i, CL);
     }
+    for (int i = 0; i < kMailSlots; ++i) mbar_init(mail0 + 8 * i, 1);
     mbar_init(q_full, 4);
     mbar_init(s_full, 1);
     mbar_init(s_full + 8, 1);
@@ -199,6 +282,9 @@ __global__ void __launch_bounds__(192, 2)
     flags[0] = 0;
     fence_mbar_init();
   }
+  // every CTA's barriers are initialised before any CTA of the cluster
+  // touches another's
+  if (CL > 1) cluster_sync();
   // Launched with programmatic dependent launch: wait for the previous kernel
   // in the stream before the tensor memory is taken, so that a CTA started
   // early never holds columns that a still-running CTA of an earlier launch
@@ -226,7 +312,7 @@ __global__ void __launch_bounds__(192, 2)
         c_nrg = 0;
     bool c_loaded = false;
     // the running count of items per sequence, 32 sequences at a time:
-    // items are (KV head, partition, row group) of each sequence
+    // items are (KV head, partition, group of CL row groups) of each sequence
     auto load_chunk = [&]() {
       const int sl = cs + lane;
       c_L = 0;
@@ -247,8 +333,8 @@ __global__ void __launch_bounds__(192, 2)
         }
       }
       const int c_np = (c_L + p.range_tokens - 1) / p.range_tokens;
-      c_nrg = (c_n + p.chunk_tokens - 1) / p.chunk_tokens;
-      c_cnt = sl < p.num_seqs ? p.num_kv_heads * c_np * c_nrg : 0;
+      c_nrg = (c_n + p.chunk_tokens - 1) / p.chunk_tokens;  // row groups
+      c_cnt = sl < p.num_seqs ? p.num_kv_heads * c_np * ((c_nrg + CL - 1) / CL) : 0;
       c_incl = c_cnt;
 #pragma unroll
       for (int off = 1; off < 32; off <<= 1) {
@@ -258,18 +344,47 @@ __global__ void __launch_bounds__(192, 2)
       c_total = __shfl_sync(0xffffffffu, c_incl, 31);
       c_loaded = true;
     };
-    auto grab_issue = [&]() -> int { return atomic_add_lane0(p.sched, lane); };
-    const int takers = (int)gridDim.x;
-    auto grab_value = [&](int raw) -> int { return takers + __shfl_sync(0xffffffffu, raw, 0); };
-    int item = blockIdx.x;
+    // The leader of a cluster takes the next item from the counter and mails
+    // it to the others (a store into their mailbox slot, then a release
+    // arrival on the slot's mbarrier); they wait for it, bounded.  The leader
+    // runs at most a few items ahead (the stage slots are freed only by every
+    // CTA), well within kMailSlots.
+    bool ok = true;
+    auto grab_issue = [&]() -> int { return rank == 0 ? atomic_add_lane0(p.sched, lane) : 0; };
+    const int takers = (int)gridDim.x / CL;
+    int ordinal = 0;  // items handed over so far
+    auto next_item = [&](int raw) -> int {
+      if (CL == 1) return takers + __shfl_sync(0xffffffffu, raw, 0);
+      // hand-over k (from 0) uses slot k % kMailSlots, the (k / kMailSlots)-th
+      // time: its phase parity
+      const int e = ordinal % kMailSlots;
+      const uint32_t par = (uint32_t)(ordinal / kMailSlots) & 1u;
+      ++ordinal;
+      int nx = 0;
+      if (rank == 0) {
+        nx = takers + __shfl_sync(0xffffffffu, raw, 0);
+        if (lane > 0 && lane < CL) {
+          st_cluster(cluster_addr(smem_u32(const_cast<int *>(mailbox) + e), (uint32_t)lane), nx);
+          mbar_arrive_remote(cluster_addr(mail0 + 8 * e, (uint32_t)lane));
+        }
+        __syncwarp();
+      } else {
+        bool w = true;
+        if (lane == 0) w = mbar_wait_cluster(mail0 + 8 * e, par, limit, flags);
+        ok = __shfl_sync(0xffffffffu, w, 0);
+        nx = ok ? mailbox[e] : -1;
+        nx = __shfl_sync(0xffffffffu, nx, 0);
+      }
+      return nx;
+    };
+    int item = (int)blockIdx.x / CL;  // a cluster's first item: its index
     int i = 0;           // stages issued
     int ik = 0, iv = 0;  // stages whose K (with the end marker) and V copies are issued
-    bool ok = true;
     while (true) {
-      int s = 0, kvh = 0, part = 0, L = 0, nrg = 0, qs = 0, n_s = 0, rg = 0;
+      int s = 0, kvh = 0, part = 0, L = 0, nrg = 0, qs = 0, n_s = 0, rg = 0, gr = 0;
       bool found = false;
       if (item < 0) {
-        if (lane == 0) report(p.status, kStatusBadInput);
+        if (lane == 0 && ok) report(p.status, kStatusBadInput);
       } else {
         while (true) {
           if (!c_loaded) load_chunk();
@@ -283,11 +398,13 @@ __global__ void __launch_bounds__(192, 2)
             n_s = __shfl_sync(0xffffffffu, c_n, ls);
             const int first = cbase + __shfl_sync(0xffffffffu, c_incl - c_cnt, ls);
             const int np_s = (L + p.range_tokens - 1) / p.range_tokens;
-            const int per_head = np_s * nrg;
+            const int ngr = (nrg + CL - 1) / CL;  // groups of CL row groups
+            const int per_head = np_s * ngr;
             kvh = (item - first) / per_head;
             const int rem = (item - first) % per_head;
-            part = rem / nrg;
-            rg = rem % nrg;
+            part = rem / ngr;
+            gr = rem % ngr;
+            rg = gr * CL + (int)rank;  // this CTA's row group (maybe past the chunk)
             found = s < p.num_seqs;
             break;
           }
@@ -300,15 +417,18 @@ __global__ void __launch_bounds__(192, 2)
       if (!found) break;
       int next_raw = 0;
       const int t_first = rg * p.chunk_tokens;
-      const int ntok = min(p.chunk_tokens, n_s - t_first);
+      const int ntok = max(0, min(p.chunk_tokens, n_s - t_first));  // 0: no rows here
       const int lim_base = L - n_s + t_first;
       const int row0 = qs + t_first;
       const int tok_begin = part * p.range_tokens;
-      const int tok_end = min(min(tok_begin + p.range_tokens, L), lim_base + ntok);
+      // the cluster's keys: up to the limit of its last row group's last token
+      const int lim_cluster = L - n_s + min(n_s, (gr * CL + CL) * p.chunk_tokens);
+      const int tok_end = min(min(tok_begin + p.range_tokens, L), lim_cluster);
       if (part == 0 && p.row_limit)
         for (int t = lane; t < ntok; t += 32) p.row_limit[row0 + t] = lim_base + t + 1;
       if (tok_end <= tok_begin) {  // the partition lies past every token of the group
-        item = grab_value(grab_issue());
+        item = next_item(grab_issue());
+        if (!ok) break;
         continue;
       }
       // a window of 64 block-table entries (lane j: pages win0 + j and
@@ -359,10 +479,16 @@ __global__ void __launch_bounds__(192, 2)
           mbar_arrive_expect_tx(fullk0 + 8 * sk, (uint32_t)__popc(valid_mask) * U * 128u * NPANELS);
         }
         __syncwarp();
-        // rows lane*U .. : groups lane*U/8 .. of the slot, every panel, one copy
-        if (y >= 0) {
+        // rows lane*U .. : groups lane*U/8 .. of the slot, every panel, one
+        // copy; in a cluster each CTA issues the units lane = rank (mod CL),
+        // multicast to every CTA (each counts all the stage's bytes)
+        const bool mine = y >= 0 && (lane % CL) == (int)rank;
+        if (mine) {
           const uint32_t kdst = kring_u32 + (uint32_t)sk * kUmmaHalf + (uint32_t)(lane * U / 8) * kUmmaGroup;
-          tma_load_4d(kdst, &tmap_k, 0, 0, 0, y >> 3, fullk0 + 8 * sk);
+          if (CL > 1)
+            tma_load_4d_multicast(kdst, &tmap_k, 0, 0, 0, y >> 3, fullk0 + 8 * sk, all_ctas);
+          else
+            tma_load_4d(kdst, &tmap_k, 0, 0, 0, y >> 3, fullk0 + 8 * sk);
         }
         ik = i + 1;
         if (i >= NV) {  // V slot: the PV of stage i - NV has read it
@@ -374,9 +500,12 @@ __global__ void __launch_bounds__(192, 2)
         if (lane == 0)
           mbar_arrive_expect_tx(fullv0 + 8 * sv, (uint32_t)__popc(valid_mask) * U * 128u * NPANELS);
         __syncwarp();
-        if (y >= 0) {
+        if (mine) {
           const uint32_t vdst = vring_u32 + (uint32_t)sv * kUmmaHalf + (uint32_t)(lane * U / 8) * kUmmaGroup;
-          tma_load_4d(vdst, &tmap_v, 0, 0, 0, y >> 3, fullv0 + 8 * sv);
+          if (CL > 1)
+            tma_load_4d_multicast(vdst, &tmap_v, 0, 0, 0, y >> 3, fullv0 + 8 * sv, all_ctas);
+          else
+            tma_load_4d(vdst, &tmap_v, 0, 0, 0, y >> 3, fullv0 + 8 * sv);
         }
         iv = i + 1;
         if (j == 0) next_raw = grab_issue();
@@ -389,7 +518,8 @@ __global__ void __launch_bounds__(192, 2)
         }
       }
       if (!ok) break;
-      item = grab_value(next_raw);
+      item = next_item(next_raw);
+      if (!ok) break;
     }
     pdl_launch_dependents();
     if (ok) {  // no more items: a K slot's header says so
@@ -485,8 +615,13 @@ __global__ void __launch_bounds__(192, 2)
           const uint64_t db = smem_desc(vst + (uint32_t)kk * 2u * kUmmaGroup, 1024, kUmmaGroup);
           tc_mma(tmem_o, da, db, kIdescPV, ((h.flags & kStageFirst) && kk == 0) ? 0u : 1u);
         }
-        tc_commit(emptyk0 + 8 * sk);  // the stage's K and P are read
-        tc_commit(emptyv0 + 8 * sv);  // and its V
+        if (CL > 1) {  // every CTA's slot counts this CTA's release
+          tc_commit_multicast(emptyk0 + 8 * sk, all_ctas);  // the stage's K and P are read
+          tc_commit_multicast(emptyv0 + 8 * sv, all_ctas);  // and its V
+        } else {
+          tc_commit(emptyk0 + 8 * sk);
+          tc_commit(emptyv0 + 8 * sv);
+        }
         if (h.flags & kStageLast) tc_commit(o_done);
         if (!s1) {
           ok = mbar_wait(fullk0 + 8 * sk1, par1, limit, flags);
@@ -741,9 +876,12 @@ __global__ void __launch_bounds__(192, 2)
     pdl_launch_dependents();
   }
 
-  // every role is done with the tensor memory: free it
+  // every role is done with the tensor memory: free it.  In a cluster, no CTA
+  // leaves while another may still copy into its shared memory or arrive on
+  // its barriers.
   tc_fence_before();
   __syncthreads();
+  if (CL > 1) cluster_sync();
   if (warp == 5) {
     tc_fence_after();
     tmem_dealloc(tmem, kUmmaTmemCols);
@@ -761,13 +899,19 @@ __global__ void __launch_bounds__(192, 2)
 
 size_t umma_chunk_smem_bytes() {
   return (size_t)(kUmmaKSlots + kUmmaVSlots) * kUmmaHalf + kUmmaQBytes +
-         kUmmaKSlots * sizeof(UmmaStage) + (2 * kUmmaKSlots + 2 * kUmmaVSlots + 8) * 8 + 32;
+         kUmmaKSlots * sizeof(UmmaStage) +
+         (2 * kUmmaKSlots + 2 * kUmmaVSlots + 8 + kMailSlots) * 8 +
+         (8 + kMailSlots) * 4;  // flags, tensor-memory address, mailbox
 }
 
-AttnKernelInfo attn_kernel_umma_chunk(int dtype_bf16) {
+AttnKernelInfo attn_kernel_umma_chunk(int dtype_bf16, bool clustered) {
   AttnKernelInfo k{};
-  k.fn = dtype_bf16 ? reinterpret_cast<const void *>(&pa_umma_chunk_kernel<__nv_bfloat16>)
-                    : reinterpret_cast<const void *>(&pa_umma_chunk_kernel<__half>);
+  if (clustered)
+    k.fn = dtype_bf16 ? reinterpret_cast<const void *>(&pa_umma_chunk_kernel<__nv_bfloat16, true>)
+                      : reinterpret_cast<const void *>(&pa_umma_chunk_kernel<__half, true>);
+  else
+    k.fn = dtype_bf16 ? reinterpret_cast<const void *>(&pa_umma_chunk_kernel<__nv_bfloat16, false>)
+                      : reinterpret_cast<const void *>(&pa_umma_chunk_kernel<__half, false>);
   k.consumer_warps = 5;  // 4 softmax warps and the MMA warp; the producer is the sixth
   k.stage_tokens = kUmmaKeys;
   k.max_group = kUmmaRows;

@@ -48,6 +48,7 @@ struct AttnParams {
   int chunk_tokens;
   int *row_limit;     // V2 chunk mode: keys visible to each query row (for Phase 2)
   int num_stages;
+  int cluster;        // tcgen05 chunk kernel: CTAs of a thread-block cluster (1: none)
   int debug_flags;
   float scale_log2;   // scale * log2(e)
   uint64_t wait_limit_ns;
@@ -101,7 +102,8 @@ struct AttnKernelInfo {
 inline bool umma_chunk_ok(int head_size, int group, long long max_rows) {
   return head_size == 128 && group >= 1 && 128 % group == 0 && max_rows > 16;
 }
-AttnKernelInfo attn_kernel_umma_chunk(int dtype_bf16);
+// clustered: the instantiation launched in thread-block clusters
+AttnKernelInfo attn_kernel_umma_chunk(int dtype_bf16, bool clustered);
 size_t umma_chunk_smem_bytes();
 constexpr int kUmmaStagesHost = 2;
 constexpr int kUmmaTmemColsHost = 256;  // tensor-memory columns per CTA (of 512 per SM)

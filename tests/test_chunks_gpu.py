@@ -169,8 +169,41 @@ def test_long_chunk_workload_full_size():
     args = (q.to(dev), c.key_cache.to(dev), c.value_cache.to(dev), c.block_tables.to(dev),
             c.seq_lens.to(dev), qs.to(dev))
     for variant in (pa.PA_VARIANT_V2, pa.PA_VARIANT_V1):
-        out = torch.full((R, H, D), float("nan"), dtype=c.dtype, device=dev)
-        pa.pa_chunks_forward(out, *args, c.scale, c.partition_size, ws,
-                             max_seq_len=c.max_seq_len, max_chunk=64, variant=variant)
+        outs = []
+        for share in (0, 1):  # 1: clusters of 4 CTAs share each K/V stage
+            out = torch.full((R, H, D), float("nan"), dtype=c.dtype, device=dev)
+            pa.pa_chunks_forward(out, *args, c.scale, c.partition_size, ws,
+                                 max_seq_len=c.max_seq_len, max_chunk=64, variant=variant,
+                                 share_kv=share)
+            assert pa.pa_read_device_status(ws) == pa.PA_OK
+            assert_close(out, ref, c.dtype, f"c4 cache, 64-token chunks, v{variant}, share {share}")
+            outs.append(out)
+        # each CTA does the same arithmetic either way; stages past a row
+        # group's own limit add exact zeros
+        assert torch.equal(outs[0], outs[1])
+
+
+TCGEN05_CASES = [c for c in CASES if c[1] == 128 and c[2] * max(c[7]) > 16]
+
+
+@pytest.mark.parametrize("dtype,D,G,Hkv,bs,P,lens,qlens", TCGEN05_CASES,
+                         ids=[f"{str(c[0])[6:]}-G{c[2]}-bs{c[4]}-P{c[5]}" for c in TCGEN05_CASES])
+@pytest.mark.parametrize("variant", [pa.PA_VARIANT_V1, pa.PA_VARIANT_V2], ids=["v1", "v2"])
+def test_shared_kv_clusters_equal_separate_loads(dtype, D, G, Hkv, bs, P, lens, qlens, variant):
+    """share_kv (the CTAs of a (sequence, KV head)'s row groups as a cluster
+    sharing each K/V stage by multicast, row groups past a short chunk left
+    empty) gives the same bits as separate loads, on every tcgen05 case."""
+    H = G * Hkv
+    c, q, qs = _chunk_case(4000 + D + G + P, lens, qlens, H, Hkv, D, dtype, bs, P)
+    R = q.shape[0]
+    ws = pa.alloc_workspace(R, H, D, c.max_seq_len, P)
+    args = (q.cuda(), c.key_cache.cuda(), c.value_cache.cuda(), c.block_tables.cuda(),
+            c.seq_lens.cuda(), qs.cuda())
+    outs = []
+    for share in (0, 1):
+        out = torch.full((R, H, D), float("nan"), dtype=dtype, device="cuda")
+        pa.pa_chunks_forward(out, *args, c.scale, P, ws, max_seq_len=c.max_seq_len,
+                             max_chunk=max(qlens), variant=variant, share_kv=share)
         assert pa.pa_read_device_status(ws) == pa.PA_OK
-        assert_close(out, ref, c.dtype, f"c4 cache, 64-token chunks, v{variant}")
+        outs.append(out)
+    assert torch.equal(outs[0], outs[1])

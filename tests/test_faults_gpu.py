@@ -63,13 +63,16 @@ def test_bounded_wait_runs_out_and_context_survives(variant, math):
     assert_close(out, reference(case), torch.bfloat16)
 
 
+@pytest.mark.parametrize("share_kv", [0, 1], ids=["own", "cluster"])
 @pytest.mark.parametrize("variant", [pa.PA_VARIANT_V1, pa.PA_VARIANT_V2])
-def test_bounded_wait_runs_out_in_the_tcgen05_chunk_kernel(variant):
+def test_bounded_wait_runs_out_in_the_tcgen05_chunk_kernel(variant, share_kv):
     """Query chunks of 40 tokens x 8 heads (320 rows per KV head: the tcgen05
     kernel) with every softmax warp waiting on a barrier nothing releases: the
     MMA thread and the producer give up in turn, the MMA thread waits for its
     own MMAs, the tensor memory is freed, PA_ERR_DEVICE_TIMEOUT is reported,
-    and the next call on the same context matches the oracle."""
+    and the next call on the same context matches the oracle; also with the
+    CTAs in clusters sharing K/V, where every CTA still meets the cluster's
+    last barrier."""
     import oracle
     c = workloads.make_case("faults_chunks", 83, 3, 16, 2, 128, torch.bfloat16, 16,
                             [900, 2000, 40], partition_size=512, extra_blocks=4)
@@ -85,11 +88,11 @@ def test_bounded_wait_runs_out_in_the_tcgen05_chunk_kernel(variant):
     out = torch.zeros(q.shape, dtype=torch.bfloat16, device="cuda")
     pa.pa_chunks_forward(out, *args, c.scale, 512, ws, max_seq_len=c.max_seq_len, max_chunk=40,
                          variant=variant, debug_flags=pa.PA_DEBUG_STALL_CONSUMERS,
-                         wait_limit_ns=200_000)
+                         wait_limit_ns=200_000, share_kv=share_kv)
     assert pa.pa_read_device_status(ws) == pa.PA_ERR_DEVICE_TIMEOUT
     torch.cuda.synchronize()  # the context is still usable
     pa.pa_chunks_forward(out, *args, c.scale, 512, ws, max_seq_len=c.max_seq_len, max_chunk=40,
-                         variant=variant)
+                         variant=variant, share_kv=share_kv)
     assert pa.pa_read_device_status(ws) == pa.PA_OK
     assert_close(out, ref, torch.bfloat16, "chunks after a timed-out call")
 
