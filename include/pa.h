@@ -106,10 +106,20 @@ typedef struct {
  * path without hanging or faulting the GPU. */
 #define PA_DEBUG_STALL_CONSUMERS 1
 
-/* Debug: query chunks never take the tcgen05 kernel (chunks of at least 128
+/* Debug: query chunks never take the tcgen05 kernel (chunks of more than 16
  * rows per KV head at head_size 128 then run on the mma.sync row-owning
  * kernel), for comparisons of the two. */
 #define PA_DEBUG_NO_TCGEN05 2
+
+/* Option: every call that the tcgen05 kernel of small items can serve takes
+ * it: head_size 128, bf16/f16, at most 16 query rows per KV head and item
+ * (decode with any group, query chunks of up to 16 / group tokens an item),
+ * without the fused combine.  The keys of a stage are the MMA's M and the
+ * item's rows its N, so no tensor-core lane computes a missing row.  Off by
+ * default: on GB300 the mma.sync kernels are faster on every such workload
+ * measured (decode with 16 query heads a KV head: 0.116-0.146 ms against
+ * 0.098 ms a step).  PA_DEBUG_NO_TCGEN05 wins over it. */
+#define PA_DEBUG_TCGEN05_KEYS 4
 
 
 /* Bytes of workspace that pa_v2_forward needs (V1 needs only the 256-byte

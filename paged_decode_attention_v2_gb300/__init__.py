@@ -35,6 +35,7 @@ PA_VARIANT_AUTO, PA_VARIANT_V1, PA_VARIANT_V2 = 0, 1, 2
 PA_MATH_AUTO, PA_MATH_SIMT, PA_MATH_TENSOR = 0, 1, 2
 PA_DEBUG_STALL_CONSUMERS = 1
 PA_DEBUG_NO_TCGEN05 = 2
+PA_DEBUG_TCGEN05_KEYS = 4
 
 _DTYPES = {torch.float32: PA_DTYPE_F32, torch.bfloat16: PA_DTYPE_BF16,
            torch.float16: PA_DTYPE_F16}

@@ -350,6 +350,35 @@ pa_status_t encode_cache_map_umma(CUtensorMap *map, const void *base, int dtype,
   return PA_OK;
 }
 
+// The queries as TMA sees them for the tcgen05 kernel of small items:
+// (element of D, head, query row), so that a box of (64, group, tokens) at
+// (64 p, kv_head * group, row) brings panel p of an item's tokens x group
+// rows, landing as [token][head][128 bytes] (row n = token * group + head) in
+// the 128-byte swizzle.
+pa_status_t encode_query_map(CUtensorMap *map, const void *query, int dtype, int head_size,
+                             int num_heads, long long rows, int group, int tokens) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc;
+  pa_status_t st = get_encoder(&enc);
+  if (st != PA_OK) return st;
+  const int elt = elt_size(dtype);
+  CUtensorMapDataType dt = dtype == PA_DTYPE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                  : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  cuuint64_t gdim[3] = {(cuuint64_t)head_size, (cuuint64_t)num_heads,
+                        (cuuint64_t)(rows > 0 ? rows : 1)};
+  cuuint64_t gstride[2] = {(cuuint64_t)head_size * elt, (cuuint64_t)num_heads * head_size * elt};
+  cuuint32_t box[3] = {(cuuint32_t)(kPanelBytes / elt), (cuuint32_t)group, (cuuint32_t)tokens};
+  cuuint32_t estride[3] = {1, 1, 1};
+  CUresult r = enc(map, dt, 3, const_cast<void *>(query), gdim, gstride, box, estride,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    char msg[64];
+    snprintf(msg, sizeof msg, "CUresult %d", (int)r);
+    return fail_cuda("cuTensorMapEncodeTiled", msg);
+  }
+  return PA_OK;
+}
+
 // Phase 2 of one call: kernel, grid and parameters.  It is planned before
 // Phase 1 is enqueued, so that nothing can fail between the two launches.
 struct Phase2Plan {
@@ -465,8 +494,19 @@ pa_status_t launch(const Call &c, bool v2, const pa_options_t &opt) {
   if (math == kMathTensor && c.dtype == PA_DTYPE_F32) return PA_ERR_UNSUPPORTED;
   const bool chunk = c.q_start != nullptr;
   if (chunk && math != kMathTensor) return PA_ERR_UNSUPPORTED;
-  const bool umma = chunk && !(opt.debug_flags & PA_DEBUG_NO_TCGEN05) &&
-                    umma_chunk_ok(c.head_size, group, (long long)c.max_chunk * group);
+  const bool tc = math == kMathTensor && !(opt.debug_flags & PA_DEBUG_NO_TCGEN05);
+  // Items of at most 16 rows on tcgen05 with the keys on the MMA's M, when
+  // asked for (PA_DEBUG_TCGEN05_KEYS), unless the combine is to be fused
+  // into Phase 1, which only the mma.sync kernels do.  Not the default:
+  // measured on GB300 (16 heads a group on the 256-sequence cache) it takes
+  // 0.123-0.146 ms (V2) / 0.116-0.126 ms (V1) a step, on two boxes, against
+  // the two-n-tile mma.sync kernel's 0.098 ms: one CTA an SM does not cover
+  // its item boundaries.
+  const long long item_rows = chunk ? (long long)c.max_chunk * group : group;
+  const bool keys = tc && (opt.debug_flags & PA_DEBUG_TCGEN05_KEYS) &&
+                    umma_keys_ok(c.head_size, item_rows) && aligned(c.query, 16) &&
+                    !(v2 && !chunk && opt.fuse_partitions > 0);
+  const bool umma = chunk && tc && umma_chunk_ok(c.head_size, group, item_rows);
   // tcgen05 chunks of several 128-row groups per KV head, when asked
   // (share_kv): a cluster of 2 or 4 CTAs takes them together, sharing each
   // stage's K/V by multicast.  Off by default: measured on GB300 (the
@@ -478,7 +518,8 @@ pa_status_t launch(const Call &c, bool v2, const pa_options_t &opt) {
     cl = rg >= 4 ? 4 : rg >= 2 ? 2 : 1;
   }
   const AttnKernelInfo k =
-      umma    ? attn_kernel_umma_chunk(c.dtype == PA_DTYPE_BF16 ? 1 : 0, cl > 1)
+      keys    ? attn_kernel_umma_keys(c.dtype == PA_DTYPE_BF16 ? 1 : 0)
+      : umma  ? attn_kernel_umma_chunk(c.dtype == PA_DTYPE_BF16 ? 1 : 0, cl > 1)
       : chunk ? (c.dtype == PA_DTYPE_BF16
                      ? attn_kernel_chunk_bf16(c.head_size, group, c.max_chunk * group)
                      : attn_kernel_chunk_f16(c.head_size, group, c.max_chunk * group))
@@ -516,8 +557,9 @@ pa_status_t launch(const Call &c, bool v2, const pa_options_t &opt) {
     }
     if (stages <= 0) return PA_ERR_UNSUPPORTED;
   }
-  size_t smem = k.umma ? umma_chunk_smem_bytes()
-                      : attn_smem_bytes(c.head_size, elt, k.stage_tokens, k.consumer_warps,
+  size_t smem = k.umma == 2 ? umma_keys_smem_bytes()
+                 : k.umma    ? umma_chunk_smem_bytes()
+                             : attn_smem_bytes(c.head_size, elt, k.stage_tokens, k.consumer_warps,
                                         k.max_group, stages, simt);
   if (smem > (size_t)dev->max_smem_optin) return PA_ERR_UNSUPPORTED;
 
@@ -529,6 +571,22 @@ pa_status_t launch(const Call &c, bool v2, const pa_options_t &opt) {
   if (st != PA_OK) return st;
   st = encode(&tmap_v, c.value_cache, c.dtype, c.head_size, rows, unit_rows);
   if (st != PA_OK) return st;
+  // the kernel of small items: an item's tokens (of its query chunk), at
+  // most 16 rows with its heads, and never more than there are query rows
+  long long item_tokens = 1;
+  if (chunk) {
+    item_tokens = k.max_group / group;
+    if (item_tokens > c.max_chunk) item_tokens = c.max_chunk;
+    if (item_tokens > c.num_rows) item_tokens = c.num_rows;
+    if (item_tokens < 1) item_tokens = 1;
+  }
+  CUtensorMap tmap_q;
+  memset(&tmap_q, 0, sizeof tmap_q);
+  if (k.umma == 2) {
+    st = encode_query_map(&tmap_q, c.query, c.dtype, c.head_size, c.num_heads, query_rows(c), group,
+                          (int)item_tokens);
+    if (st != PA_OK) return st;
+  }
 
   uint8_t *ws = static_cast<uint8_t *>(c.workspace);
   const int max_parts = v2 ? max_parts_of(c.max_seq_len, c.partition_size) : 1;
@@ -586,7 +644,8 @@ pa_status_t launch(const Call &c, bool v2, const pa_options_t &opt) {
   if (chunk) {
     p.q_start = c.q_start;
     p.num_rows = c.num_rows;
-    p.chunk_tokens = k.max_group / group;  // tokens of an item: its rows / heads per token
+    // tokens of an item: its rows / heads per token
+    p.chunk_tokens = k.umma == 2 ? (int)item_tokens : k.max_group / group;
   }
   p.num_stages = stages;
   p.debug_flags = opt.debug_flags;
@@ -622,7 +681,7 @@ pa_status_t launch(const Call &c, bool v2, const pa_options_t &opt) {
   if (per_sm < 1) return PA_ERR_UNSUPPORTED;
   if (opt.ctas_per_sm > 0 && opt.ctas_per_sm < per_sm) per_sm = opt.ctas_per_sm;
   if (k.umma) {
-    // The occupancy query answers 1 for this kernel whatever its shared
+    // The occupancy query answers 1 for these kernels whatever its shared
     // memory (measured on GB300: at 20 KB too), while two CTAs fit its
     // registers, shared memory and tensor memory and do run side by side
     // (1.5x the throughput of one).  So its CTAs per SM come from those
@@ -633,7 +692,8 @@ pa_status_t launch(const Call &c, bool v2, const pa_options_t &opt) {
     if (st != PA_OK) return st;
     if (est > per_sm) per_sm = est;
     if (opt.ctas_per_sm > 0 && opt.ctas_per_sm < per_sm) per_sm = opt.ctas_per_sm;
-    if (per_sm * kUmmaTmemColsHost > 512) per_sm = 512 / kUmmaTmemColsHost;
+    const int tmem_cols = k.umma == 2 ? kUmmaKeysTmemColsHost : kUmmaTmemColsHost;
+    if (per_sm * tmem_cols > 512) per_sm = 512 / tmem_cols;
   }
   const long long range_parts =
       v2 ? (long long)(c.part_end < p.max_parts ? c.part_end : p.max_parts) - c.part_begin
@@ -667,7 +727,7 @@ pa_status_t launch(const Call &c, bool v2, const pa_options_t &opt) {
       pattr[1].val.clusterDim.z = 1;
       cfg.numAttrs = 2;
     }
-    void *args[3] = {&p, &tmap_k, &tmap_v};
+    void *args[4] = {&p, &tmap_k, &tmap_v, &tmap_q};  // the query map: small-item kernel only
     cudaError_t e = cudaLaunchKernelExC(&cfg, k.fn, args);
     if (e != cudaSuccess) return fail_cuda("launch attention kernel", e);
   }

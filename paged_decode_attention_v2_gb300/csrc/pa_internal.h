@@ -90,7 +90,9 @@ struct AttnKernelInfo {
   int stage_tokens;   // tokens of one ring stage
                       // (consumer_warps * kTileTokens, or 64 for row-owning warps)
   int max_group;      // largest H / Hkv it handles (query chunks: rows of an item)
-  int umma;           // 1: the tcgen05 query-chunk kernel (its own layout and launch)
+  int umma;           // tcgen05 kernels (their own layouts and launches): 1 the
+                      // query-chunk kernel (rows on M), 2 the kernel of small
+                      // items (keys on M)
 };
 
 // Query chunks on tcgen05: D 128, 16-bit, more than 16 rows per KV head.  A
@@ -105,8 +107,16 @@ inline bool umma_chunk_ok(int head_size, int group, long long max_rows) {
 // clustered: the instantiation launched in thread-block clusters
 AttnKernelInfo attn_kernel_umma_chunk(int dtype_bf16, bool clustered);
 size_t umma_chunk_smem_bytes();
+// Items of at most 16 query rows on tcgen05, the keys on the MMA's M (decode
+// with up to 16 heads a KV head, short query chunks): D 128, 16-bit.
+inline bool umma_keys_ok(int head_size, long long item_rows) {
+  return head_size == 128 && item_rows >= 1 && item_rows <= 16;
+}
+AttnKernelInfo attn_kernel_umma_keys(int dtype_bf16);
+size_t umma_keys_smem_bytes();
 constexpr int kUmmaStagesHost = 2;
-constexpr int kUmmaTmemColsHost = 256;  // tensor-memory columns per CTA (of 512 per SM)
+constexpr int kUmmaTmemColsHost = 256;     // tensor-memory columns per CTA (of 512 per SM)
+constexpr int kUmmaKeysTmemColsHost = 64;  // the same for the kernel of small items
 
 // Dynamic shared memory the attention kernel needs for `stages` stages (the
 // kernel's carve-up, in order: the ring of stages, each its K and V bytes and
