@@ -194,3 +194,16 @@ def test_keys_out_of_range_block_id_is_reported(variant):
     assert pa.pa_read_device_status(dc.ws) == pa.PA_ERR_DEVICE_BAD_INPUT
     assert_close(dc.run(variant=variant, debug_flags=KEYS), reference(case), torch.bfloat16,
                  "after bad input")
+
+
+@pytest.mark.parametrize("variant", [pa.PA_VARIANT_V2, pa.PA_VARIANT_V1], ids=["v2", "v1"])
+def test_keys_gqa16_full_size(variant):
+    """At full size on the 16-head-group decode workload (the 256-sequence
+    lengths and cache shape with 32 query / 2 KV heads): every output against
+    the oracle, V2 and V1."""
+    c = dict(workloads.CONFIGS["c4_batch256"])
+    c.pop("index")
+    c["num_kv_heads"] = 2
+    case = workloads.make_case("gqa16", workloads.SEED_BASE + 77, **c)
+    assert_close(DeviceCase(case).run(variant=variant, debug_flags=KEYS), reference(case),
+                 case.dtype, f"G=16 full size v{variant}")
