@@ -385,6 +385,8 @@ struct Phase2Plan {
   ReduceParams r;
   const void *fn = nullptr;
   long long ctas = 0;
+  int threads = 256;
+  size_t smem = 0;  // dynamic shared memory
 };
 
 pa_status_t plan_phase2(const Call &c, const AttnParams &p, const DeviceFacts *dev,
@@ -405,6 +407,29 @@ pa_status_t plan_phase2(const Call &c, const AttnParams &p, const DeviceFacts *d
   r.max_seq_len = c.max_seq_len;
   r.fuse_limit = p.fuse_limit;
   r.row_limit = p.row_limit;
+  // Rows whose partials fit in 8 KB (and 32 partitions, one a lane): a warp
+  // takes each row's partials in one bulk copy, the next row's in flight
+  // while it reduces the current one, so that the whole batch crosses the
+  // memory system in about one round trip (measured on GB300, the
+  // 256-sequence decode batch: see the kernel's notes).
+  if (p.max_parts <= 32 && (size_t)p.max_parts * c.head_size * 4 <= 8192) {
+    const void *fn = reduce_rows_kernel(c.dtype);
+    if (!fn) return PA_ERR_UNSUPPORTED;
+    const size_t smem = reduce_rows_smem_bytes(p.max_parts, c.head_size);
+    pa_status_t st = ensure_smem(fn, smem);
+    if (st != PA_OK) return st;
+    int occ_r = 0;
+    st = occupancy(fn, kReduceRowsThreads, smem, &occ_r);
+    if (st != PA_OK) return st;
+    if (occ_r < 1) return PA_ERR_UNSUPPORTED;
+    long long ctas = (prows + kReduceRowsThreads / 32 - 1) / (kReduceRowsThreads / 32);
+    if (ctas > (long long)occ_r * dev->sm_count) ctas = (long long)occ_r * dev->sm_count;
+    out->fn = fn;
+    out->ctas = ctas;
+    out->threads = kReduceRowsThreads;
+    out->smem = smem;
+    return PA_OK;
+  }
   // Team size W (warps per task) and column split: the pair that minimises
   // the chain of the longest task (1 + its rounds of loads, a round being one
   // batch of NB partitions per thread) plus 2 for every further wave of
@@ -467,8 +492,8 @@ pa_status_t launch_phase2(const Phase2Plan &plan, cudaStream_t stream) {
   cudaLaunchConfig_t cfg;
   memset(&cfg, 0, sizeof cfg);
   cfg.gridDim = dim3((unsigned)plan.ctas, 1, 1);
-  cfg.blockDim = dim3(256, 1, 1);
-  cfg.dynamicSmemBytes = 0;
+  cfg.blockDim = dim3((unsigned)plan.threads, 1, 1);
+  cfg.dynamicSmemBytes = plan.smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

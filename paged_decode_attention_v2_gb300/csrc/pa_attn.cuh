@@ -42,8 +42,6 @@
 
 namespace pa {
 
-constexpr int kStatusBadInput = 5;  // PA_ERR_DEVICE_BAD_INPUT
-constexpr int kStatusTimeout = 6;   // PA_ERR_DEVICE_TIMEOUT
 constexpr int kDebugStallConsumers = 1;
 
 constexpr int kStageFirst = 1;  // first stage of an item (carries the queries)

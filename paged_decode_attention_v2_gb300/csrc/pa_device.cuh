@@ -11,6 +11,20 @@
 
 namespace pa {
 
+// status codes the kernels record (the device values of pa_status_t)
+constexpr int kStatusBadInput = 5;  // PA_ERR_DEVICE_BAD_INPUT
+constexpr int kStatusTimeout = 6;   // PA_ERR_DEVICE_TIMEOUT
+
+// Phase 2: the partitions of (sequence, head) row `row` (query chunks: of the
+// row's own visible keys, a Phase 1 result), never more than the workspace
+// holds a row: a length out of range (Phase 1 reported it), or a row limit
+// that Phase 1 left unwritten (a row it rejected), is clamped
+__device__ __forceinline__ int partitions_of_row(const ReduceParams &p, long long row) {
+  int L = p.row_limit ? __ldcg(p.row_limit + row / p.num_heads) : __ldg(p.seq_lens + row / p.num_heads);
+  L = L < 0 ? 0 : (L > p.max_seq_len ? p.max_seq_len : L);
+  return (L + p.partition_size - 1) / p.partition_size;
+}
+
 // ---------------------------------------------------------------------------
 // Status word: the first kernel to see a problem records it; later ones keep
 // the first code.

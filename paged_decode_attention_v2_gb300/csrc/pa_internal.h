@@ -148,6 +148,11 @@ AttnKernelInfo attn_kernel_simt_f16(int head_size, int group);
 AttnKernelInfo attn_kernel_chunk_bf16(int head_size, int group, int max_rows);
 AttnKernelInfo attn_kernel_chunk_f16(int head_size, int group, int max_rows);
 const void *reduce_kernel(int dtype, int float4_per_thread);
+// Phase 2 for rows whose partials fit in a few KB (bulk copies into shared
+// memory, four warps a CTA, one row a warp at a time)
+constexpr int kReduceRowsThreads = 128;
+const void *reduce_rows_kernel(int dtype);
+size_t reduce_rows_smem_bytes(int max_parts, int head_size);
 const void *stage_in_kernel();
 
 }  // namespace pa

@@ -38,16 +38,6 @@ __device__ __forceinline__ void team_sync(int g, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(1 + g), "r"(nthreads) : "memory");
 }
 
-__device__ __forceinline__ int partitions_of(const ReduceParams &p, long long row) {
-  if (p.row_limit) {  // query chunks: the row's own visible keys (a Phase 1 result)
-    const int Lr = __ldcg(p.row_limit + row / p.num_heads);
-    return (Lr + p.partition_size - 1) / p.partition_size;
-  }
-  int L = __ldg(p.seq_lens + row / p.num_heads);
-  L = L < 0 ? 0 : (L > p.max_seq_len ? p.max_seq_len : L);  // Phase 1 reported it
-  return (L + p.partition_size - 1) / p.partition_size;
-}
-
 template <typename OutT, int VPT>
 __global__ void __launch_bounds__(kReduceThreads, 4)
     pa_v2_reduce_kernel(const __grid_constant__ ReduceParams p) {
@@ -74,21 +64,21 @@ __global__ void __launch_bounds__(kReduceThreads, 4)
   // waiting for Phase 1 (programmatic dependent launch), later ones a task
   // ahead.
   // (in chunk mode the counts are Phase 1 results: read after the wait)
-  int np_next = task < ntasks && !p.row_limit ? partitions_of(p, task / dsplit) : 0;
+  int np_next = task < ntasks && !p.row_limit ? partitions_of_row(p, task / dsplit) : 0;
   pdl_wait_primary();
   // Phase 1 has completed: its work counters go back to zero for the next call
   if (p.sched && blockIdx.x == 0 && threadIdx.x == 0) {
     p.sched[0] = 0;
     p.sched[1] = 0;
   }
-  if (p.row_limit && task < ntasks) np_next = partitions_of(p, task / dsplit);
+  if (p.row_limit && task < ntasks) np_next = partitions_of_row(p, task / dsplit);
   pdl_launch_dependents();  // the next kernel still waits for this grid to complete
 
   for (; task < ntasks; task += tstride) {
     const long long row = task / dsplit;  // s * num_heads + h
     const int col0 = (int)(task % dsplit) * ncols;
     int np = np_next;
-    if (task + tstride < ntasks) np_next = partitions_of(p, (task + tstride) / dsplit);
+    if (task + tstride < ntasks) np_next = partitions_of_row(p, (task + tstride) / dsplit);
     // With the combine fused into Phase 1 (fuse_limit > 0) it finished these
     // sequences, empty ones included; without it, this kernel writes the
     // zeros of empty sequences.
